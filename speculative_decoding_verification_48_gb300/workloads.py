@@ -1,0 +1,298 @@
+"""Seeded synthetic inputs for speculative-sampling verification.
+
+This module only *creates* inputs: logits, draft tokens, temperatures,
+uniform draws and token trees.  It holds none of the verification arithmetic
+(no accept test, no residual, no argmax walk), so the library and the float64
+oracle used by the tests can both consume its output without sharing code.
+
+Every batch row (or tree) is drawn from its own Philox stream keyed by
+``(seed, row)``, so any subset of rows can be regenerated on its own.  Values
+are drawn in float32/float64 and rounded to the storage dtype by
+``torch.Tensor.to`` (round to nearest even); consumers read the rounded
+values back.
+
+Draft tokens are drawn from the draft distribution q = softmax(draft / T)
+with the Gumbel-max trick (argmax of draft/T plus Gumbel noise), which is
+an exact sampler of q; greedy rows (T <= 0) use the draft's own top token.
+That is draft generation (step 1 of the method), not verification.
+
+Workloads (the pages measure on XSum, HumanEval, WMT and Alpaca; these
+synthetic shapes stand in for them):
+  c1  chain, B=256 rounds, gamma=4, V=1000, fp32; target ~ N(0, 2^2),
+      draft = target + N(0, 0.5^2), T = 1.
+  c2  chain, 4096 rounds, gamma=5, V=32000, bf16; Zipf-biased target
+      N(0,1) - 1.1 ln(rank), draft = target + N(0,1), T in {0, 0.7, 1.0}.
+  c3  chain, B=64, gamma=7, V=128256, bf16; Zipf-biased target, per-row draft
+      noise sigma ~ U[0.3, 2.0], per-row T ~ U[0, 1.2) with T = 0 on rows
+      b % 8 == 0 (greedy rows).
+  c4  token trees, 16 trees x 64 nodes, depth <= 8, 1..4 children per node,
+      fp16 node logits ~ N(0, 2^2), one planted root path matching the
+      target argmax with probability 0.8 per step.
+  c5  chain, B=256, gamma=4, V=256000; bf16 Zipf-biased target at T = 0.8;
+      draft given as fp32 probabilities softmax(target + N(0, 0.7^2)) (the
+      input data, computed here once); rows b % 16 == 0 have their accept
+      draws set to 0 (all drafts accepted, bonus token drawn).
+"""
+
+from __future__ import annotations
+
+from collections import deque
+from dataclasses import dataclass, field
+from typing import Callable, Optional, Sequence
+
+import numpy as np
+import torch
+
+DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
+
+
+def rng_for(seed: int, *keys: int) -> np.random.Generator:
+    """Philox stream keyed by (seed, *keys)."""
+    return np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, *keys])))
+
+
+def round_to(x: np.ndarray, dtype: str) -> torch.Tensor:
+    """Round float data to the storage dtype (round to nearest even)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DTYPES[dtype])
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    """Stored values as float64 numpy (exact for fp32 / bf16 / fp16)."""
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def zipf_bias(seed: int, V: int) -> np.ndarray:
+    """-1.1 * ln(rank(x)) with rank = perm(x) + 1, one permutation per seed."""
+    perm = rng_for(seed, 0x7FFFFFFF).permutation(V)
+    return (-1.1 * np.log(perm.astype(np.float64) + 1.0)).astype(np.float32)
+
+
+@dataclass
+class ChainCase:
+    name: str
+    target: torch.Tensor          # [B, gamma+1, V] storage dtype (CPU)
+    draft: torch.Tensor           # [B, gamma, V] logits, or fp32 probabilities
+    draft_is_probs: bool
+    draft_tokens: torch.Tensor    # int32 [B, gamma]
+    temperatures: torch.Tensor    # fp32 [B]
+    uniforms: torch.Tensor        # fp32 [B, gamma+1]
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def B(self): return self.target.shape[0]
+    @property
+    def gamma(self): return self.target.shape[1] - 1
+    @property
+    def V(self): return self.target.shape[2]
+
+    def select(self, rows: Sequence[int]) -> "ChainCase":
+        idx = torch.as_tensor(list(rows), dtype=torch.long)
+        return ChainCase(self.name, self.target[idx].contiguous(), self.draft[idx].contiguous(),
+                         self.draft_is_probs, self.draft_tokens[idx].contiguous(),
+                         self.temperatures[idx].contiguous(), self.uniforms[idx].contiguous(),
+                         dict(self.meta))
+
+    def numpy64(self):
+        """Arguments for the float64 oracle, in its argument order."""
+        return (to_f64(self.target), to_f64(self.draft), self.draft_is_probs,
+                self.draft_tokens.numpy().astype(np.int64),
+                to_f64(self.temperatures), to_f64(self.uniforms))
+
+
+@dataclass
+class TreeCase:
+    name: str
+    node_logits: torch.Tensor     # [B, N, V] storage dtype (CPU)
+    parent: torch.Tensor          # int32 [B, N]
+    node_tokens: torch.Tensor     # int32 [B, N]
+    max_depth: int
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def B(self): return self.node_logits.shape[0]
+    @property
+    def N(self): return self.node_logits.shape[1]
+    @property
+    def V(self): return self.node_logits.shape[2]
+
+    def numpy64(self):
+        return (to_f64(self.node_logits), self.parent.numpy().astype(np.int64),
+                self.node_tokens.numpy().astype(np.int64), self.max_depth)
+
+
+def make_chain(name: str, seed: int, B: int, gamma: int, V: int, dtype: str = "bf16",
+               target: str = "zipf", target_sigma: float = 1.0,
+               draft_sigma: tuple = (1.0, 1.0),
+               temperature: Callable[[int, np.random.Generator], float] | float = 1.0,
+               draft_probs: bool = False, draft_probs_T: float = 1.0,
+               force_accept_every: int = 0) -> ChainCase:
+    """General chain workload; every row b uses the Philox stream (seed, b).
+
+    target: "zipf" -> N(0, target_sigma^2) - 1.1 ln(rank); "normal" ->
+    N(0, target_sigma^2).  Draft logits = target (before rounding) + N(0, s_b^2)
+    with s_b ~ U[draft_sigma].  ``temperature`` is a constant or a callable
+    (b, rng) -> T.  With ``draft_probs`` the draft is stored as fp32
+    probabilities softmax((target + noise) / draft_probs_T) and the target
+    keeps the row temperature.
+    """
+    bias = zipf_bias(seed, V) if target == "zipf" else None
+    tgt = torch.empty((B, gamma + 1, V), dtype=DTYPES[dtype])
+    ddt = "f32" if draft_probs else dtype
+    dft = torch.empty((B, gamma, V), dtype=DTYPES[ddt])
+    toks = np.empty((B, gamma), np.int32)
+    temps = np.empty(B, np.float32)
+    unif = np.empty((B, gamma + 1), np.float32)
+    for b in range(B):
+        rng = rng_for(seed, b)
+        base = rng.standard_normal((gamma + 1, V), dtype=np.float32) * np.float32(target_sigma)
+        if bias is not None:
+            base += bias
+        s_b = rng.uniform(draft_sigma[0], draft_sigma[1])
+        dl = base[:gamma] + rng.standard_normal((gamma, V), dtype=np.float32) * np.float32(s_b)
+        T = temperature(b, rng) if callable(temperature) else float(temperature)
+        temps[b] = T
+        unif[b] = rng.random(gamma + 1, dtype=np.float32)
+        if force_accept_every and b % force_accept_every == 0:
+            unif[b, :gamma] = 0.0
+        gumbel = rng.gumbel(size=(gamma, V))
+        tgt[b] = round_to(base, dtype)
+        if draft_probs:
+            z = dl.astype(np.float64) / draft_probs_T
+            z -= z.max(axis=1, keepdims=True)
+            e = np.exp(z)
+            probs = (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+            dft[b] = torch.from_numpy(probs)
+            with np.errstate(divide="ignore"):
+                toks[b] = np.argmax(np.log(probs.astype(np.float64)) + gumbel, axis=1)
+        else:
+            dft[b] = round_to(dl, dtype)
+            dr = to_f64(dft[b])
+            if T <= 0:
+                toks[b] = np.argmax(dr, axis=1)
+            else:
+                toks[b] = np.argmax(dr / T + gumbel, axis=1)
+    return ChainCase(name, tgt, dft, draft_probs, torch.from_numpy(toks),
+                     torch.from_numpy(temps), torch.from_numpy(unif),
+                     dict(seed=seed, dtype=dtype, draft_dtype=ddt))
+
+
+# ---------------------------------------------------------------------------
+# The five workloads
+# ---------------------------------------------------------------------------
+
+def c1_chain_fp32_v1000(rounds: int = 256, seed: int = 1001) -> ChainCase:
+    return make_chain("c1_chain_B1x256rounds_g4_V1000_f32", seed, rounds, 4, 1000, "f32",
+                      target="normal", target_sigma=2.0, draft_sigma=(0.5, 0.5),
+                      temperature=1.0)
+
+
+def c2_chain_bf16_v32000(T: float, rounds: int = 4096, seed: int = 1002) -> ChainCase:
+    return make_chain(f"c2_chain_B1x{rounds}rounds_g5_V32000_bf16_T{T}", seed, rounds, 5, 32000,
+                      "bf16", target="zipf", draft_sigma=(1.0, 1.0), temperature=float(T))
+
+
+def _c3_temperature(b: int, rng: np.random.Generator) -> float:
+    T = rng.uniform(0.0, 1.2)
+    return 0.0 if b % 8 == 0 else T
+
+
+def c3_chain_bf16_v128256(B: int = 64, gamma: int = 7, V: int = 128256,
+                          seed: int = 1003) -> ChainCase:
+    return make_chain(f"c3_chain_B{B}_g{gamma}_V{V}_bf16", seed, B, gamma, V, "bf16",
+                      target="zipf", draft_sigma=(0.3, 2.0), temperature=_c3_temperature)
+
+
+def c5_chain_bf16_probs_v256000(B: int = 256, gamma: int = 4, V: int = 256000,
+                                seed: int = 1005) -> ChainCase:
+    return make_chain(f"c5_chain_B{B}_g{gamma}_V{V}_bf16_f32probs", seed, B, gamma, V, "bf16",
+                      target="zipf", draft_sigma=(0.7, 0.7), temperature=0.8,
+                      draft_probs=True, draft_probs_T=1.0, force_accept_every=16)
+
+
+def make_tree(name: str, seed: int, B: int = 16, N: int = 64, V: int = 32000,
+              max_depth: int = 8, kmin: int = 1, kmax: int = 4, dtype: str = "f16",
+              sigma: float = 2.0, p_match: float = 0.8) -> TreeCase:
+    """Token trees given as parent-index arrays (BFS numbering, parent[n] < n).
+
+    Each node gets kmin..kmax children until N nodes exist; no node deeper than
+    ``max_depth``.  Sibling tokens are distinct.  Along one random root-to-leaf
+    path, each step is planted: with probability ``p_match`` the parent's logit
+    row is raised at the child's token (to the row maximum + 1) so the target's
+    top token is that child; otherwise the parent's logit at the child's token
+    is set below the row minimum so the child does not match.
+    """
+    logits = torch.empty((B, N, V), dtype=DTYPES[dtype])
+    parents = np.empty((B, N), np.int32)
+    tokens = np.empty((B, N), np.int32)
+    for b in range(B):
+        rng = rng_for(seed, b)
+        par, dep = [-1], [0]
+        queue = deque([0])
+        while len(par) < N:
+            if not queue:
+                queue = deque(n for n in range(len(par)) if dep[n] < max_depth)
+                if not queue:
+                    raise ValueError("tree cannot reach N nodes within max_depth")
+            n = queue.popleft()
+            if dep[n] >= max_depth:
+                continue
+            k = int(rng.integers(kmin, kmax + 1))
+            for _ in range(k):
+                if len(par) >= N:
+                    break
+                par.append(n)
+                dep.append(dep[n] + 1)
+                queue.append(len(par) - 1)
+        par_a = np.asarray(par, np.int32)
+        children = [np.flatnonzero(par_a == n) for n in range(N)]
+        tok = np.empty(N, np.int32)
+        tok[0] = rng.integers(0, V)
+        for n in range(N):
+            if len(children[n]):
+                tok[children[n]] = rng.choice(V, size=len(children[n]), replace=False)
+        lg = rng.standard_normal((N, V), dtype=np.float32) * np.float32(sigma)
+        cur = 0
+        while len(children[cur]):
+            c = int(rng.choice(children[cur]))
+            if rng.random() < p_match:
+                lg[cur, tok[c]] = lg[cur].max() + 1.0
+            else:
+                lg[cur, tok[c]] = lg[cur].min() - 1.0
+            cur = c
+        logits[b] = round_to(lg, dtype)
+        parents[b] = par_a
+        tokens[b] = tok
+    return TreeCase(name, logits, torch.from_numpy(parents), torch.from_numpy(tokens),
+                    max_depth, dict(seed=seed, dtype=dtype))
+
+
+def c4_tree_f16_v32000(B: int = 16, N: int = 64, V: int = 32000, seed: int = 1004) -> TreeCase:
+    return make_tree(f"c4_tree_B{B}_N{N}_V{V}_f16", seed, B, N, V, max_depth=8)
+
+
+# Algorithmic bytes: every logit byte the verification needs, read once.
+
+def chain_algorithmic_bytes(case: ChainCase, num_accepted: Optional[np.ndarray] = None) -> int:
+    """Target rows of every batch row; draft logit rows of stochastic rows;
+    in probability mode the draft row at the rejected position only (needs
+    the call's ``num_accepted``); plus draft tokens, temperatures, uniforms."""
+    B, g, V = case.B, case.gamma, case.V
+    te = case.target.element_size()
+    de = case.draft.element_size()
+    T = case.temperatures.numpy()
+    stoch = T > 0
+    nbytes = B * (g + 1) * V * te
+    if case.draft_is_probs:
+        if num_accepted is not None:
+            rej = stoch & (np.asarray(num_accepted) < g)
+            nbytes += int(rej.sum()) * V * de
+        nbytes += int(stoch.sum()) * g * de         # gathers q(x)
+    else:
+        nbytes += int(stoch.sum()) * g * V * de
+    nbytes += B * g * 4 + B * 4 + B * (g + 1) * 4
+    return int(nbytes)
+
+
+def tree_algorithmic_bytes(case: TreeCase) -> int:
+    B, N, V = case.B, case.N, case.V
+    return int(B * N * V * case.node_logits.element_size() + 2 * B * N * 4)
