@@ -1,0 +1,459 @@
+"""Benchmark of the GB300 verification library.
+
+One step = one spec_verify_chain call over one batch of the batched
+128K-vocabulary chain workload (B=64, gamma=7, V=128256, bf16 logits,
+per-row temperatures with 8 greedy rows): temperature softmax statistics of
+every row, accept tests, first-reject scan, residual / bonus draws (all of
+the chain hot path; the tree path is measured in ``other_workloads``).
+
+Metric: verified draft positions per second (B * gamma per step), with the
+achieved HBM bandwidth (algorithmic logit bytes / call time) against the
+measured copy bandwidth in MEASURED_PEAKS.json.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c3|c5|c2|c1] [--quick]
+
+Under torchrun (N > 1) every rank verifies its own batch (rows r*B ..
+(r+1)*B - 1 of the same synthetic stream): weak scaling with no collective
+on the data path; a barrier brackets the timed region and rank 0 reports
+the max time over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_verification_48_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s vs 8 TB/s (1 GB300)"
+UNIT = "positions/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["c3", "c5", "c2", "c1"], default="c3")
+    ap.add_argument("--quick", action="store_true", help="skip the other workloads")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    return ap.parse_args()
+
+
+def make_workload(name: str, row0: int = 0):
+    if name == "c3":
+        return W.make_chain("c3_chain_B64_g7_V128256_bf16", 1003, 64, 7, 128256, "bf16",
+                            target="zipf", draft_sigma=(0.3, 2.0),
+                            temperature=W._c3_temperature, row0=row0)
+    if name == "c5":
+        return W.make_chain("c5_chain_B256_g4_V256000_bf16_f32probs", 1005, 256, 4, 256000,
+                            "bf16", target="zipf", draft_sigma=(0.7, 0.7), temperature=0.8,
+                            draft_probs=True, force_accept_every=16, row0=row0)
+    if name == "c2":
+        return W.make_chain("c2_chain_B1_g5_V32000_bf16_T1.0", 1002, 1, 5, 32000, "bf16",
+                            target="zipf", temperature=1.0, row0=row0)
+    if name == "c1":
+        return W.make_chain("c1_chain_B1_g4_V1000_f32", 1001, 1, 4, 1000, "f32",
+                            target="normal", target_sigma=2.0, draft_sigma=(0.5, 0.5),
+                            temperature=1.0, row0=row0)
+    raise ValueError(name)
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_48_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per call from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    sha = re.search(r"kernel_source_sha:\s*(\w+)", txt)
+    val = re.search(r"dram_bytes_per_call:\s*([0-9.eE+]+)", txt)
+    if not sha or not val or sha.group(1) != kernel_source_sha():
+        return None
+    return float(val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class ChainCall:
+    """Raw C-ABI call of spec_verify_chain with fixed device buffers."""
+
+    def __init__(self, sv, case, dev, stream):
+        self.case = case
+        self.sv = sv
+        B, g, V = case.B, case.gamma, case.V
+        self.dev_in = [case.target.to(dev), case.draft.to(dev), case.draft_tokens.to(dev),
+                       case.temperatures.to(dev), case.uniforms.to(dev)]
+        self.out = [torch.empty((B, g + 1), dtype=torch.int32, device=dev),
+                    torch.empty((B,), dtype=torch.int32, device=dev),
+                    torch.empty((B, g, 4), dtype=torch.float32, device=dev),
+                    torch.empty((B,), dtype=torch.int32, device=dev)]
+        rows = (g + 1) + (0 if case.draft_is_probs else g)
+        dt = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+        nb = sv.spec_verify_workspace_bytes(B, rows, V, dt[case.target.dtype])
+        self.ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+        self.stream = stream
+        t, d, x, T, u = self.dev_in
+        self.args = (ctypes.c_void_p(t.data_ptr()), dt[t.dtype], ctypes.c_void_p(d.data_ptr()),
+                     dt[d.dtype], int(case.draft_is_probs), ctypes.c_void_p(x.data_ptr()),
+                     ctypes.c_void_p(T.data_ptr()), ctypes.c_void_p(u.data_ptr()), B, g, V,
+                     ctypes.c_void_p(self.out[0].data_ptr()),
+                     ctypes.c_void_p(self.out[1].data_ptr()),
+                     ctypes.c_void_p(self.out[2].data_ptr()),
+                     ctypes.c_void_p(self.out[3].data_ptr()),
+                     ctypes.c_void_p(self.ws.data_ptr()), ctypes.c_size_t(nb),
+                     ctypes.c_void_p(stream.cuda_stream))
+        self.fn = sv.lib().spec_verify_chain
+
+    def __call__(self):
+        st = self.fn(*self.args)
+        if st != 0:
+            raise RuntimeError(self.sv.spec_verify_status_string(st))
+
+
+def time_calls(call, steps, warmup, stream, per_call_events=True):
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)] if per_call_events else None
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(steps):
+            if ev:
+                ev[i][0].record(stream)
+            call()
+            if ev:
+                ev[i][1].record(stream)
+        t1.record(stream)
+    torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    per = [a.elapsed_time(b) for a, b in ev] if ev else [total_ms / steps]
+    return total_ms, float(np.mean(per)), float(np.median(per))
+
+
+def bench_chain_e2e(sv, case, dev, stream, steps):
+    """Host buffers in, host results out: H2D of the step's inputs from pinned
+    memory, the C-ABI call, D2H of tokens and counts, host sync, per step."""
+    host_in = [t.pin_memory() for t in (case.target, case.draft, case.draft_tokens,
+                                         case.temperatures, case.uniforms)]
+    call = ChainCall(sv, case, dev, stream)
+    host_out = [torch.empty_like(call.out[0], device="cpu").pin_memory(),
+                torch.empty_like(call.out[1], device="cpu").pin_memory()]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        with torch.cuda.stream(stream):
+            for d, h in zip(call.dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            call()
+            host_out[0].copy_(call.out[0], non_blocking=True)
+            host_out[1].copy_(call.out[1], non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        step()
+    t = time.perf_counter()
+    for _ in range(steps):
+        step()
+    dt = time.perf_counter() - t
+    return dt, h2d, d2h
+
+
+def other_workloads(sv, dev, stream, peak):
+    """Secondary measurements: the other chain workloads and the tree."""
+    out = {}
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    for name, steps in (("c5", 200), ("c2", 2000), ("c1", 2000)):
+        case = make_workload(name)
+        call = ChainCall(sv, case, dev, stream)
+        call()
+        torch.cuda.synchronize()
+        nacc = call.out[1].cpu().numpy()
+        nbytes = W.chain_algorithmic_bytes(case, nacc)
+        # flush L2 between calls for the small workloads; time each call alone
+        times = []
+        for i in range(min(steps, 200)):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = float(np.median(times))
+        out[case.name] = {"us_per_call": ms * 1e3, "positions_per_s": case.B * case.gamma / (ms * 1e-3),
+                          "GBps": nbytes / (ms * 1e-3) / 1e9, "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
+                          "algorithmic_bytes": nbytes, "l2": "flushed before each call"}
+    tree = W.c4_tree_f16_v32000()
+    args = [t.to(dev) for t in (tree.node_logits, tree.parent, tree.node_tokens)]
+    res = sv.spec_verify_tree_greedy(*args, tree.max_depth, stream=stream)
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(tree.B, tree.N, tree.V, 2), dtype=torch.uint8,
+                     device=dev)
+    times = []
+    for i in range(200):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        sv.spec_verify_tree_greedy(*args, tree.max_depth, out_path=res[0], out_tokens=res[1],
+                                   out_num_accepted=res[2], out_row_status=res[3], workspace=ws,
+                                   stream=stream)
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = float(np.median(times))
+    nbytes = W.tree_algorithmic_bytes(tree)
+    out[tree.name] = {"us_per_call": ms * 1e3, "positions_per_s": tree.B * (tree.N - 1) / (ms * 1e-3),
+                      "GBps": nbytes / (ms * 1e-3) / 1e9, "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
+                      "algorithmic_bytes": nbytes, "l2": "flushed before each call"}
+    del flush
+    return out
+
+
+def cpu_baseline(case, rows):
+    """The float64 oracle as it stands, single process, on `rows` batch rows."""
+    import oracle
+    sub = case.select(rows)
+    args = sub.numpy64()
+    t = time.perf_counter()
+    oracle.verify_chain(*args)
+    dt = time.perf_counter() - t
+    return len(rows) * case.gamma / dt, dt
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(a, world, rank):
+    """The oracle on the host cores, same workload, metric and unit; each step
+    verifies one batch row of it (a bounded sample)."""
+    if rank != 0:
+        return
+    case = make_workload(a.workload)
+    import oracle
+    B = case.B
+    budget_s = 120.0
+    one = case.select([0]).numpy64()
+    t = time.perf_counter()
+    oracle.verify_chain(*one)
+    row_s = time.perf_counter() - t
+    steps = max(3, min(a.steps, int(budget_s / max(row_s, 1e-6))))
+    warm = min(a.warmup, 3)
+    for i in range(warm):
+        oracle.verify_chain(*case.select([i % B]).numpy64())
+    args = [case.select([i % B]).numpy64() for i in range(steps)]
+    t = time.perf_counter()
+    for x in args:
+        oracle.verify_chain(*x)
+    dt = time.perf_counter() - t
+    value = steps * case.gamma / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": a.gpus, "steps": steps, "steps_requested": a.steps, "warmup": warm,
+            "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "global_batch": B, "gamma": case.gamma,
+                       "V": case.V, "step_sample": "one batch row per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{steps} batch rows of {case.name}, one per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    a = parse()
+    world, rank, local = dist_setup(a.gpus)
+    if a.impl == "reference":
+        run_reference(a, world, rank)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    from speculative_decoding_verification_48_gb300 import build
+    build.build()
+    import speculative_decoding_verification_48_gb300 as sv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    peak, peak_kind = measured_peak()
+
+    case = make_workload(a.workload, row0=rank * 100000)
+    call = ChainCall(sv, case, dev, stream)
+    call()
+    torch.cuda.synchronize()
+    nacc = call.out[1].cpu().numpy()
+    alg_bytes = W.chain_algorithmic_bytes(case, nacc)
+    positions = case.B * case.gamma
+    l2_bytes = 129 * 1024 * 1024
+    input_bytes = sum(t.numel() * t.element_size() for t in call.dev_in)
+
+    barrier(world)
+    with ClockSampler(local) as clk:
+        total_ms, mean_call_ms, med_call_ms = time_calls(call, a.steps, a.warmup, stream)
+    barrier(world)
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / a.steps
+    value = world * positions * a.steps / (total_ms * 1e-3)
+
+    e2e_dt, h2d, d2h = bench_chain_e2e(sv, case, dev, stream, a.e2e_steps)
+    e2e_dt = max_over_ranks(e2e_dt, world, dev)
+    e2e_value = world * positions * a.e2e_steps / e2e_dt
+
+    achieved = alg_bytes / (mean_call_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": case.meta["dtype"],
+        "data": "synthetic (seeded; stands in for the pages' XSum/HumanEval/WMT workloads)",
+        "config": {"workload": case.name, "global_batch": case.B * world, "gamma": case.gamma,
+                   "V": case.V, "seq_len": None, "parallelism": f"independent batch rows x{world}",
+                   "l2": (f"inputs larger than L2 ({input_bytes / 1e6:.0f} MB > "
+                          f"{l2_bytes / 1e6:.0f} MB)" if input_bytes > 2 * l2_bytes else
+                          "inputs smaller than 2x L2")},
+        "positions_per_step": positions,
+        "algorithmic_bytes_per_call": alg_bytes,
+        "call_us_mean": mean_call_ms * 1e3, "call_us_median": med_call_ms * 1e3,
+        "hbm_GBps": achieved, "frac_of_8TBps_nominal": achieved / 8000.0,
+        "mean_accepted": float(nacc.mean()),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "traffic": ncu_traffic(a.workload),
+                     "kernel": "spec_verify_chain call (Phase-A + Phase-B launches)"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": a.e2e_steps},
+        "gpu_launches": 2 * a.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1:
+        rows = list(range(min(case.B, 24)))
+        v, dt = cpu_baseline(case, rows)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{len(rows)} of {case.B} batch rows of {case.name} "
+                                          f"({dt:.1f} s, single process)"}
+        if not a.quick:
+            line["other_workloads"] = other_workloads(sv, dev, stream, peak)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,184 @@
+/*
+ * spec_verify.h — C ABI of the GB300 (sm_103a) speculative-sampling
+ * verification library.
+ *
+ * The library runs the verification step of speculative decoding on one GPU:
+ *
+ *   - chain speculative sampling ("Speculative Sampling", Chen et al.,
+ *     arXiv:2302.01318, as explained on "論文解説: Speculative Sampling —
+ *     ドラフトモデルによるLLMデコード高速化", §技術的詳細 ステップ3 and
+ *     §修正付き棄却サンプリング): temperature softmax of target and draft rows,
+ *     accept test min(1, p/q) against a supplied uniform, stop at the first
+ *     rejection, draw the replacement from norm(max(0, p - q)), or a bonus
+ *     token from p at position gamma+1 when every draft is accepted;
+ *   - greedy chain verification ("投機的デコーディングとは？LLMの回答を高速化
+ *     する仕組み", §ドラフト生成と並列検証の仕組み and the worked example in
+ *     §候補の採用と棄却を具体例で見る);
+ *   - SpecInfer-style token-tree greedy verification (SpecInfer explainer,
+ *     §技術の仕組み › 基本アイデア and §推論方法): argmax per tree node, then a
+ *     walk from the root along children whose token matches.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All array pointers are DEVICE pointers owned by the caller.  Arrays are
+ *    dense and row-major: a logit row is V contiguous elements, row stride V.
+ *    The library never allocates and never synchronises the host; work is
+ *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *  - `workspace` is caller-owned device memory of at least
+ *    spec_verify_workspace_bytes(...) bytes, 16-byte aligned, ZERO-FILLED
+ *    before its first use (e.g. cudaMemsetAsync).  Every call that completes
+ *    leaves its counter words at zero again, so a workspace can be reused by
+ *    later calls in stream order without clearing.  Calls that may overlap on
+ *    the GPU need distinct workspaces.  After a row reports SV_ROW_TIMEOUT the
+ *    workspace must be zero-filled again before reuse.
+ *  - Row alignment is the caller's job: target row i scores draft i (the
+ *    distribution conditioned on the context and drafts 0..i-1); row gamma is
+ *    the bonus row.
+ *  - Host-detectable argument errors return a status synchronously and
+ *    enqueue nothing.  Errors in the DATA (bad token ids, NaN rows, malformed
+ *    trees) are reported per row in `out_row_status` (bit mask SV_ROW_*); such
+ *    a row gets num_accepted = 0 and every token -1.
+ *  - Every pointer must be aligned to its element type (out_diag to 16
+ *    bytes); otherwise the call returns SV_ERR_INVALID_ARG.  16-byte vector
+ *    loads are used when a row starts on a 16-byte boundary; other rows take
+ *    a scalar path.  Any V >= 1 is accepted.
+ *  - No function throws; all are thread-safe given distinct workspaces.
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SV_API __attribute__((visibility("default")))
+#else
+#define SV_API
+#endif
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, workspace too small */
+  SV_ERR_UNSUPPORTED = 2,   /* dtype combination or size the library does not handle */
+  SV_ERR_CUDA = 3,          /* a CUDA runtime call or kernel launch failed */
+  SV_ERR_TIMEOUT = 4        /* reserved: device-side timeouts are reported per row */
+} sv_status;
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1, SV_F16 = 2 } sv_dtype;
+
+/* Per-row data-error bits written to out_row_status. */
+#define SV_ROW_OK 0
+#define SV_ROW_BAD_TOKEN 1        /* a draft / node token outside [0, V) */
+#define SV_ROW_NONFINITE 2        /* NaN (or +inf / all -inf) in a softmax row, NaN in an argmax row,
+                                     a non-finite draft probability read, or a non-finite residual */
+#define SV_ROW_BAD_TREE 4         /* parent[0] != -1 or parent[n] outside [0, n) */
+#define SV_ROW_TIMEOUT 8          /* a bounded device-side wait ran out (about one second) */
+#define SV_ROW_BAD_TEMPERATURE 16 /* temperature NaN or in (0, 1e-20) */
+
+/* Size limits checked on the host. */
+#define SV_MAX_GAMMA 31           /* gamma + 1 <= 32: one warp lane per position */
+#define SV_MAX_TREE_NODES 1024
+#define SV_MAX_TREE_DEPTH 31
+#define SV_MAX_VOCAB (1 << 26)
+
+/* A cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *sv_stream_t;
+
+/*
+ * Workspace bytes for B batch rows (chains or trees) of at most
+ * `rows_per_batch` logit rows of V elements each.  rows_per_batch is
+ * 2*gamma+1 for spec_verify_chain with draft logits, gamma+1 for
+ * spec_verify_chain with draft probabilities and for
+ * spec_verify_chain_greedy, and N for spec_verify_tree_greedy.  `dt` is the
+ * logit dtype.  Returns 0 for non-positive sizes.
+ */
+SV_API size_t spec_verify_workspace_bytes(int B, int rows_per_batch, int V, sv_dtype dt);
+
+/*
+ * Chain speculative sampling, one verification step per batch row.
+ * ("論文解説: Speculative Sampling", §技術的詳細 ステップ3: accept equation;
+ *  §修正付き棄却サンプリング: residual equation; §期待される高速化: gamma+1
+ *  tokens per round, hence the bonus draw.)
+ *
+ *  target_logits  [B, gamma+1, V] of dtype tdt.
+ *  draft          [B, gamma, V]: logits of dtype ddt, or, if draft_is_probs,
+ *                 fp32 probabilities (ddt must be SV_F32) used as given — no
+ *                 temperature, no renormalisation; only q(x_i) and the row at
+ *                 a rejected position are read.
+ *  draft_tokens   int32 [B, gamma].
+ *  temperatures   fp32 [B].  T <= 0: greedy row (target argmax, draft row and
+ *                 uniforms unused).  T > 0: p = softmax(target/T) and, for
+ *                 draft logits, q = softmax(draft/T).
+ *  uniforms       fp32 [B, gamma+1] in [0, 1): column i < gamma is the accept
+ *                 draw of draft i, column gamma the single categorical draw.
+ *  Per row: accept draft i iff u_i * q_i(x_i) < p_i(x_i), in order; j = first
+ *  rejection (else gamma); the token at slot j is the smallest k with
+ *  sum_{x<=k} w(x) > u_gamma * sum_x w(x), w = max(0, p_j - q_j) if j < gamma
+ *  (w = p_j if that mass is zero), w = p_gamma if j == gamma.
+ *  out_tokens       int32 [B, gamma+1]: drafts 0..j-1, the drawn token, then -1.
+ *  out_num_accepted int32 [B]: j.
+ *  out_diag         nullable fp32 [B, gamma, 4]: per draft i, (p_i(x_i),
+ *                   q_i(x_i), min(1, p/q), residual mass sum max(0, p_j - q_j)
+ *                   at i == j of a rejected row, else 0).  Zero for greedy rows.
+ *  out_row_status   nullable int32 [B]: SV_ROW_* bits, 0 when the row is valid.
+ *  Limits: B >= 1, 1 <= gamma <= SV_MAX_GAMMA, 1 <= V <= SV_MAX_VOCAB.
+ */
+SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt,
+                                   const void *draft, sv_dtype ddt, int draft_is_probs,
+                                   const int32_t *draft_tokens, const float *temperatures,
+                                   const float *uniforms, int B, int gamma, int V,
+                                   int32_t *out_tokens, int32_t *out_num_accepted,
+                                   float *out_diag, int32_t *out_row_status,
+                                   void *workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/*
+ * Greedy chain verification ("投機的デコーディングとは？", §ドラフト生成と並列検証の
+ * 仕組み; worked example §候補の採用と棄却を具体例で見る).
+ *  a_i = argmax of target row i (lowest index among equal maxima, -0 == +0);
+ *  accept while x_i == a_i; at the first mismatch j (or j = gamma) emit a_j.
+ *  target_logits [B, gamma+1, V] of dtype tdt; draft_tokens int32 [B, gamma];
+ *  out_tokens int32 [B, gamma+1]; out_num_accepted int32 [B];
+ *  out_row_status nullable int32 [B].  Same results as spec_verify_chain with
+ *  every temperature <= 0.
+ */
+SV_API sv_status spec_verify_chain_greedy(const void *target_logits, sv_dtype tdt,
+                                          const int32_t *draft_tokens, int B, int gamma, int V,
+                                          int32_t *out_tokens, int32_t *out_num_accepted,
+                                          int32_t *out_row_status, void *workspace,
+                                          size_t workspace_bytes, sv_stream_t stream);
+
+/*
+ * Token-tree greedy verification (SpecInfer explainer, §技術の仕組み › 基本アイデア,
+ * §推論方法).
+ *  node_logits [B*N, V] of dtype dt: row b*N + n scores what follows node n of
+ *  tree b.  parent int32 [B, N]: parent[0] = -1, 0 <= parent[n] < n (node 0
+ *  is the root, the context's last token; it is never verified).
+ *  node_tokens int32 [B, N].
+ *  Walk: cur = 0; while depth < max_depth: take the lowest-index child c of
+ *  cur with node_tokens[c] == argmax(row cur); stop if none.  The argmax of
+ *  the last node reached is appended as the correction / bonus token.
+ *  out_path   int32 [B, max_depth+1]: accepted node ids, then -1.
+ *  out_tokens int32 [B, max_depth+1]: accepted node tokens, the appended
+ *             token, then -1.
+ *  out_num_accepted int32 [B]: accepted depth.  out_row_status nullable [B].
+ *  Limits: 1 <= N <= SV_MAX_TREE_NODES, 0 <= max_depth <= SV_MAX_TREE_DEPTH.
+ */
+SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
+                                         const int32_t *parent, const int32_t *node_tokens,
+                                         int B, int N, int V, int max_depth,
+                                         int32_t *out_path, int32_t *out_tokens,
+                                         int32_t *out_num_accepted, int32_t *out_row_status,
+                                         void *workspace, size_t workspace_bytes,
+                                         sv_stream_t stream);
+
+/* Static description of a status code; never NULL. */
+SV_API const char *spec_verify_status_string(sv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H_ */

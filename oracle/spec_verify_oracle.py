@@ -44,7 +44,9 @@ the plainest reading, stated at the function that uses it:
   * Data errors make a row report a nonzero status, ``num_accepted = 0`` and
     all tokens -1: a draft / node token outside [0, V), a NaN (or +inf /
     all -inf) row in a softmax, a NaN in an argmax row, a malformed tree,
-    or a temperature that is NaN or in (0, 1e-20).
+    or a temperature that is NaN or in (0, 1e-20).  Draft rows given as
+    probabilities are checked only where they are read: q(x_i) for every
+    draft, and the residual mass at a rejected position (NaN propagates).
 
 Parity status: every function here is pinned by the CPU tests (closed forms,
 distribution tests, brute force and the pages' worked examples).  The exact
@@ -222,13 +224,16 @@ def verify_chain(target_logits, draft, draft_is_probs, draft_tokens,
             q = dr[s]
         else:
             q = tempered_softmax(dr[s], Ts[:, None])
-        bad = ~np.all(np.isfinite(p), axis=(1, 2))
-        bad |= ~np.all(np.isfinite(q), axis=(1, 2))
-        status[s[bad]] |= ROW_NONFINITE
-
         x = xs[s]
         px = np.take_along_axis(p[:, :gamma, :], x[..., None], axis=2)[..., 0]
         qx = np.take_along_axis(q, x[..., None], axis=2)[..., 0]
+        bad = ~np.all(np.isfinite(p), axis=(1, 2))
+        if draft_is_probs:
+            # given probabilities are only read at q(x_i) and, after a
+            # rejection, over row j (checked through the residual mass below)
+            bad |= ~np.all(np.isfinite(qx), axis=1)
+        else:
+            bad |= ~np.all(np.isfinite(q), axis=(1, 2))
         accept = u[s, :gamma] * qx < px                             # step 2
         j = np.where(accept.all(axis=1), gamma, (~accept).argmax(axis=1))  # step 3
 
@@ -244,6 +249,8 @@ def verify_chain(target_logits, draft, draft_is_probs, draft_tokens,
         rejected = j < gamma
         w = np.where(rejected[:, None], resid, pj)
         Rres = np.cumsum(resid, axis=-1)[:, -1]
+        bad |= rejected & np.isnan(Rres)
+        status[s[bad]] |= ROW_NONFINITE
         zero_mass = rejected & ~(Rres > 0)
         w = np.where(zero_mass[:, None], pj, w)
         k, C, R = inverse_cdf(w, u[s, gamma])

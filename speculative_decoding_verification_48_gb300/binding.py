@@ -1,0 +1,253 @@
+"""Thin Python binding of libspec_verify.so (ctypes).
+
+Argument marshalling only: every step of verification runs in the library's
+CUDA kernels.  Functions take CUDA tensors (contiguous, on one device),
+allocate outputs when none are given, and enqueue on the current torch
+stream of that device (or ``stream=``, a raw cudaStream_t integer).  There
+is no CPU fallback: if the library is missing these functions raise.
+
+The names and argument order follow include/spec_verify.h.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH
+
+SV_F32, SV_BF16, SV_F16 = 0, 1, 2
+_DT = {torch.float32: SV_F32, torch.bfloat16: SV_BF16, torch.float16: SV_F16}
+
+SV_ROW_OK = 0
+SV_ROW_BAD_TOKEN = 1
+SV_ROW_NONFINITE = 2
+SV_ROW_BAD_TREE = 4
+SV_ROW_TIMEOUT = 8
+SV_ROW_BAD_TEMPERATURE = 16
+
+_lib = None
+_lib_lock = threading.Lock()
+
+_VP, _I32P, _F32P = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_INT, _SIZE = ctypes.c_int, ctypes.c_size_t
+
+
+class SpecVerifyError(RuntimeError):
+    """A library call returned a status other than SV_OK."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {spec_verify_status_string(status)}")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libspec_verify.so once; raise if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"libspec_verify.so not found at {LIB_PATH}; build it with "
+                    "`python -m speculative_decoding_verification_48_gb300.build` "
+                    "(there is no CPU fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            L.spec_verify_workspace_bytes.argtypes = [_INT, _INT, _INT, _INT]
+            L.spec_verify_workspace_bytes.restype = _SIZE
+            L.spec_verify_chain.argtypes = [_VP, _INT, _VP, _INT, _INT, _I32P, _F32P, _F32P,
+                                            _INT, _INT, _INT, _I32P, _I32P, _F32P, _I32P,
+                                            _VP, _SIZE, _VP]
+            L.spec_verify_chain.restype = _INT
+            L.spec_verify_chain_greedy.argtypes = [_VP, _INT, _I32P, _INT, _INT, _INT, _I32P,
+                                                   _I32P, _I32P, _VP, _SIZE, _VP]
+            L.spec_verify_chain_greedy.restype = _INT
+            L.spec_verify_tree_greedy.argtypes = [_VP, _INT, _I32P, _I32P, _INT, _INT, _INT,
+                                                  _INT, _I32P, _I32P, _I32P, _I32P, _VP,
+                                                  _SIZE, _VP]
+            L.spec_verify_tree_greedy.restype = _INT
+            L.spec_verify_status_string.argtypes = [_INT]
+            L.spec_verify_status_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def spec_verify_status_string(status: int) -> str:
+    return lib().spec_verify_status_string(int(status)).decode()
+
+
+def spec_verify_workspace_bytes(B: int, rows_per_batch: int, V: int, dtype: int = SV_BF16) -> int:
+    return int(lib().spec_verify_workspace_bytes(int(B), int(rows_per_batch), int(V), int(dtype)))
+
+
+# ---------------------------------------------------------------------------
+# Workspace cache: one zero-filled buffer per (device, stream), grown on
+# demand.  The library leaves it zeroed after every call, so it is reused
+# by later calls on the same stream without clearing.
+# ---------------------------------------------------------------------------
+
+_ws_cache: dict = {}
+_ws_lock = threading.Lock()
+
+
+def workspace_for(device: torch.device, stream_ptr: int, nbytes: int) -> torch.Tensor:
+    key = (device.index, stream_ptr)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+        return ws
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: torch.Tensor, name: str, dtype=None, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+
+
+def _stream_ptr(device: torch.device, stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def spec_verify_chain(target_logits: torch.Tensor, draft: torch.Tensor,
+                      draft_tokens: torch.Tensor, temperatures: torch.Tensor,
+                      uniforms: torch.Tensor, draft_is_probs: bool = False,
+                      out_tokens=None, out_num_accepted=None, out_diag=None,
+                      out_row_status=None, want_diag: bool = True, workspace=None,
+                      stream=None):
+    """Chain speculative sampling (see spec_verify_chain in spec_verify.h).
+
+    Returns (tokens int32 [B, gamma+1], num_accepted int32 [B],
+    diag fp32 [B, gamma, 4] or None, row_status int32 [B])."""
+    dev = target_logits.device
+    B, G1, V = target_logits.shape
+    g = G1 - 1
+    _check(target_logits, "target_logits", device=dev)
+    if target_logits.dtype not in _DT:
+        raise TypeError("target_logits dtype must be float32, bfloat16 or float16")
+    _check(draft, "draft", shape=(B, g, V), device=dev)
+    if draft_is_probs and draft.dtype != torch.float32:
+        raise TypeError("draft probabilities must be float32")
+    if draft.dtype not in _DT:
+        raise TypeError("draft dtype must be float32, bfloat16 or float16")
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, g), dev)
+    _check(temperatures, "temperatures", torch.float32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B, G1), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_diag is None and want_diag:
+        out_diag = torch.empty((B, g, 4), dtype=torch.float32, device=dev)
+    if out_row_status is None:
+        out_row_status = torch.empty((B,), dtype=torch.int32, device=dev)
+    rows = G1 + (0 if draft_is_probs else g)
+    sp = _stream_ptr(dev, stream)
+    nbytes = spec_verify_workspace_bytes(B, rows, V, _DT[target_logits.dtype])
+    if workspace is None:
+        workspace = workspace_for(dev, sp, nbytes)
+    st = lib().spec_verify_chain(
+        target_logits.data_ptr(), _DT[target_logits.dtype], draft.data_ptr(), _DT[draft.dtype],
+        int(bool(draft_is_probs)), draft_tokens.data_ptr(), temperatures.data_ptr(),
+        uniforms.data_ptr(), B, g, V, out_tokens.data_ptr(), out_num_accepted.data_ptr(),
+        _ptr(out_diag), _ptr(out_row_status), workspace.data_ptr(), workspace.numel(), sp)
+    if st != 0:
+        raise SpecVerifyError(st, "spec_verify_chain")
+    return out_tokens, out_num_accepted, out_diag, out_row_status
+
+
+def spec_verify_chain_greedy(target_logits: torch.Tensor, draft_tokens: torch.Tensor,
+                             out_tokens=None, out_num_accepted=None, out_row_status=None,
+                             workspace=None, stream=None):
+    """Greedy chain verification.  Returns (tokens, num_accepted, row_status)."""
+    dev = target_logits.device
+    B, G1, V = target_logits.shape
+    g = G1 - 1
+    _check(target_logits, "target_logits", device=dev)
+    if target_logits.dtype not in _DT:
+        raise TypeError("target_logits dtype must be float32, bfloat16 or float16")
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, g), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, G1), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_row_status is None:
+        out_row_status = torch.empty((B,), dtype=torch.int32, device=dev)
+    sp = _stream_ptr(dev, stream)
+    nbytes = spec_verify_workspace_bytes(B, G1, V, _DT[target_logits.dtype])
+    if workspace is None:
+        workspace = workspace_for(dev, sp, nbytes)
+    st = lib().spec_verify_chain_greedy(
+        target_logits.data_ptr(), _DT[target_logits.dtype], draft_tokens.data_ptr(), B, g, V,
+        out_tokens.data_ptr(), out_num_accepted.data_ptr(), _ptr(out_row_status),
+        workspace.data_ptr(), workspace.numel(), sp)
+    if st != 0:
+        raise SpecVerifyError(st, "spec_verify_chain_greedy")
+    return out_tokens, out_num_accepted, out_row_status
+
+
+def spec_verify_tree_greedy(node_logits: torch.Tensor, parent: torch.Tensor,
+                            node_tokens: torch.Tensor, max_depth: int, out_path=None,
+                            out_tokens=None, out_num_accepted=None, out_row_status=None,
+                            workspace=None, stream=None):
+    """Token-tree greedy verification.  node_logits is [B, N, V] (or [B*N, V]
+    with ``parent`` giving B and N).  Returns (path, tokens, num_accepted,
+    row_status)."""
+    dev = node_logits.device
+    B, N = parent.shape
+    V = node_logits.shape[-1]
+    _check(node_logits, "node_logits", device=dev)
+    if node_logits.numel() != B * N * V:
+        raise ValueError("node_logits must hold B*N rows of V entries")
+    if node_logits.dtype not in _DT:
+        raise TypeError("node_logits dtype must be float32, bfloat16 or float16")
+    _check(parent, "parent", torch.int32, (B, N), dev)
+    _check(node_tokens, "node_tokens", torch.int32, (B, N), dev)
+    W = int(max_depth) + 1
+    if out_path is None:
+        out_path = torch.empty((B, W), dtype=torch.int32, device=dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, W), dtype=torch.int32, device=dev)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_row_status is None:
+        out_row_status = torch.empty((B,), dtype=torch.int32, device=dev)
+    sp = _stream_ptr(dev, stream)
+    nbytes = spec_verify_workspace_bytes(B, N, V, _DT[node_logits.dtype])
+    if workspace is None:
+        workspace = workspace_for(dev, sp, nbytes)
+    st = lib().spec_verify_tree_greedy(
+        node_logits.data_ptr(), _DT[node_logits.dtype], parent.data_ptr(),
+        node_tokens.data_ptr(), B, N, V, int(max_depth), out_path.data_ptr(),
+        out_tokens.data_ptr(), out_num_accepted.data_ptr(), _ptr(out_row_status),
+        workspace.data_ptr(), workspace.numel(), sp)
+    if st != 0:
+        raise SpecVerifyError(st, "spec_verify_tree_greedy")
+    return out_path, out_tokens, out_num_accepted, out_row_status

@@ -1,0 +1,196 @@
+// C ABI of the verification library: argument validation, workspace layout,
+// parameter packing and dispatch.  Every check that can fail happens before
+// the first CUDA call, so an invalid call touches no GPU state.
+#include <atomic>
+
+#include "sv_internal.h"
+
+namespace sv {
+
+int sm_count(int device) {
+  static std::atomic<int> cache[64];
+  if (device < 0 || device >= 64) return 0;
+  int v = cache[device].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+    cache[device].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+static bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16 || d == SV_F16; }
+
+static size_t dtype_size(int d) { return d == SV_F32 ? 4 : 2; }
+
+// Natural alignment of a (nullable) pointer.
+static bool aligned_to(const void *p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// Units are counted in 32-bit integers on the device.
+static bool units_fit(long long B, long long per_batch) {
+  return B * per_batch < (1LL << 30);
+}
+
+static void fill_workspace(KParams &P, void *ws, const Layout &L) {
+  char *w = static_cast<char *>(ws);
+  P.hdr = reinterpret_cast<WsHeader *>(w);
+  P.a_count = reinterpret_cast<unsigned *>(w + L.a_count);
+  P.b_count = reinterpret_cast<unsigned *>(w + L.b_count);
+  P.flag = reinterpret_cast<unsigned *>(w + L.flag);
+  P.dec = reinterpret_cast<Decision *>(w + L.dec);
+  P.partA = reinterpret_cast<float2 *>(w + L.partA);
+  P.partB = reinterpret_cast<float *>(w + L.partB);
+  P.tiles = L.tiles;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+SV_API size_t spec_verify_workspace_bytes(int B, int rows_per_batch, int V, sv_dtype dt) {
+  (void)dt;
+  if (B <= 0 || rows_per_batch <= 0 || V <= 0 || V > SV_MAX_VOCAB) return 0;
+  return make_layout(B, rows_per_batch, V).total;
+}
+
+SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt, const void *draft,
+                                   sv_dtype ddt, int draft_is_probs, const int32_t *draft_tokens,
+                                   const float *temperatures, const float *uniforms, int B,
+                                   int gamma, int V, int32_t *out_tokens,
+                                   int32_t *out_num_accepted, float *out_diag,
+                                   int32_t *out_row_status, void *workspace,
+                                   size_t workspace_bytes, sv_stream_t stream) {
+  if (!target_logits || !draft || !draft_tokens || !temperatures || !uniforms || !out_tokens ||
+      !out_num_accepted || !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (B < 1 || gamma < 1 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB)
+    return SV_ERR_INVALID_ARG;
+  if (!valid_dtype(tdt) || !valid_dtype(ddt)) return SV_ERR_INVALID_ARG;
+  const bool probs = draft_is_probs != 0;
+  if (probs && ddt != SV_F32) return SV_ERR_UNSUPPORTED;
+  if (!aligned_to(target_logits, dtype_size(tdt)) || !aligned_to(draft, dtype_size(ddt)) ||
+      !aligned_to(draft_tokens, 4) || !aligned_to(temperatures, 4) || !aligned_to(uniforms, 4) ||
+      !aligned_to(out_tokens, 4) || !aligned_to(out_num_accepted, 4) ||
+      !aligned_to(out_row_status, 4) || !aligned_to(out_diag, 16))
+    return SV_ERR_INVALID_ARG;
+  const int rows = (gamma + 1) + (probs ? 0 : gamma);
+  const Layout L = make_layout(B, rows, V);
+  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15))
+    return SV_ERR_INVALID_ARG;
+  if (!units_fit(B, (long long)rows * L.tiles)) return SV_ERR_UNSUPPORTED;
+
+  KParams P{};
+  P.target = target_logits;
+  P.draft = draft;
+  P.draft_tokens = draft_tokens;
+  P.temps = temperatures;
+  P.unif = uniforms;
+  P.B = B;
+  P.gamma = gamma;
+  P.V = V;
+  P.rows = rows;
+  P.phase_b = 1;
+  P.out_tokens = out_tokens;
+  P.out_nacc = out_num_accepted;
+  P.out_diag = out_diag;
+  P.out_status = out_row_status;
+  fill_workspace(P, workspace, L);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (tdt) {
+    case SV_F32: return launch_chain_f32(P, ddt, probs, s);
+    case SV_BF16: return launch_chain_bf16(P, ddt, probs, s);
+    case SV_F16: return launch_chain_f16(P, ddt, probs, s);
+  }
+  return SV_ERR_UNSUPPORTED;
+}
+
+SV_API sv_status spec_verify_chain_greedy(const void *target_logits, sv_dtype tdt,
+                                          const int32_t *draft_tokens, int B, int gamma, int V,
+                                          int32_t *out_tokens, int32_t *out_num_accepted,
+                                          int32_t *out_row_status, void *workspace,
+                                          size_t workspace_bytes, sv_stream_t stream) {
+  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted || !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (B < 1 || gamma < 1 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB)
+    return SV_ERR_INVALID_ARG;
+  if (!valid_dtype(tdt)) return SV_ERR_INVALID_ARG;
+  if (!aligned_to(target_logits, dtype_size(tdt)) || !aligned_to(draft_tokens, 4) ||
+      !aligned_to(out_tokens, 4) || !aligned_to(out_num_accepted, 4) ||
+      !aligned_to(out_row_status, 4))
+    return SV_ERR_INVALID_ARG;
+  const int rows = gamma + 1;
+  const Layout L = make_layout(B, rows, V);
+  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15))
+    return SV_ERR_INVALID_ARG;
+  if (!units_fit(B, (long long)rows * L.tiles)) return SV_ERR_UNSUPPORTED;
+
+  KParams P{};
+  P.target = target_logits;
+  P.draft_tokens = draft_tokens;
+  P.B = B;
+  P.gamma = gamma;
+  P.V = V;
+  P.rows = rows;
+  P.phase_b = 0;
+  P.out_tokens = out_tokens;
+  P.out_nacc = out_num_accepted;
+  P.out_status = out_row_status;
+  fill_workspace(P, workspace, L);
+  return launch_chain_greedy(P, tdt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
+                                         const int32_t *parent, const int32_t *node_tokens, int B,
+                                         int N, int V, int max_depth, int32_t *out_path,
+                                         int32_t *out_tokens, int32_t *out_num_accepted,
+                                         int32_t *out_row_status, void *workspace,
+                                         size_t workspace_bytes, sv_stream_t stream) {
+  if (!node_logits || !parent || !node_tokens || !out_path || !out_tokens || !out_num_accepted ||
+      !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || N > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_VOCAB || max_depth < 0 ||
+      max_depth > SV_MAX_TREE_DEPTH)
+    return SV_ERR_INVALID_ARG;
+  if (!valid_dtype(dt)) return SV_ERR_INVALID_ARG;
+  if (!aligned_to(node_logits, dtype_size(dt)) || !aligned_to(parent, 4) ||
+      !aligned_to(node_tokens, 4) || !aligned_to(out_path, 4) || !aligned_to(out_tokens, 4) ||
+      !aligned_to(out_num_accepted, 4) || !aligned_to(out_row_status, 4))
+    return SV_ERR_INVALID_ARG;
+  const Layout L = make_layout(B, N, V);
+  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15))
+    return SV_ERR_INVALID_ARG;
+  if (!units_fit(B, (long long)N * L.tiles)) return SV_ERR_UNSUPPORTED;
+
+  KParams P{};
+  P.target = node_logits;
+  P.parent = parent;
+  P.node_tokens = node_tokens;
+  P.B = B;
+  P.N = N;
+  P.V = V;
+  P.rows = N;
+  P.max_depth = max_depth;
+  P.phase_b = 0;
+  P.out_path = out_path;
+  P.out_tokens = out_tokens;
+  P.out_nacc = out_num_accepted;
+  P.out_status = out_row_status;
+  fill_workspace(P, workspace, L);
+  return launch_tree(P, dt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SV_API const char *spec_verify_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "SV_OK: success";
+    case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: null pointer, size out of range or workspace too small";
+    case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED: dtype combination or size not supported";
+    case SV_ERR_CUDA: return "SV_ERR_CUDA: a CUDA call or kernel launch failed";
+    case SV_ERR_TIMEOUT: return "SV_ERR_TIMEOUT: a device-side wait ran out";
+  }
+  return "unknown sv_status";
+}
+
+}  // extern "C"

@@ -1,0 +1,8 @@
+// Chain speculative-sampling kernels with f32 target logits.
+#include "sv_launch.cuh"
+
+namespace sv {
+sv_status launch_chain_f32(const KParams &P, sv_dtype ddt, bool probs, cudaStream_t stream) {
+  return launch_chain_t<SV_F32>(P, ddt, probs, stream);
+}
+}  // namespace sv

@@ -5,16 +5,16 @@ uniform draws and token trees.  It holds none of the verification arithmetic
 (no accept test, no residual, no argmax walk), so the library and the float64
 oracle used by the tests can both consume its output without sharing code.
 
-Every batch row (or tree) is drawn from its own Philox stream keyed by
-``(seed, row)``, so any subset of rows can be regenerated on its own.  Values
-are drawn in float32/float64 and rounded to the storage dtype by
+Every batch row (or tree) is drawn from its own torch CPU generator seeded
+from ``(seed, row)``, so any subset of rows can be regenerated on its own.
+Values are drawn in float32 and rounded to the storage dtype by
 ``torch.Tensor.to`` (round to nearest even); consumers read the rounded
 values back.
 
 Draft tokens are drawn from the draft distribution q = softmax(draft / T)
-with the Gumbel-max trick (argmax of draft/T plus Gumbel noise), which is
-an exact sampler of q; greedy rows (T <= 0) use the draft's own top token.
-That is draft generation (step 1 of the method), not verification.
+with ``torch.multinomial`` (draft generation, step 1 of the method, as in the
+pages' own drafting loop); greedy rows (T <= 0) use the draft's own top
+token.  None of this is verification.
 
 Workloads (the pages measure on XSum, HumanEval, WMT and Alpaca; these
 synthetic shapes stand in for them):
@@ -46,14 +46,27 @@ import torch
 DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
-def rng_for(seed: int, *keys: int) -> np.random.Generator:
-    """Philox stream keyed by (seed, *keys)."""
-    return np.random.Generator(np.random.Philox(np.random.SeedSequence([seed, *keys])))
+def seed_for(*keys: int) -> int:
+    """63-bit seed derived from the integer keys (SeedSequence mixing)."""
+    st = np.random.SeedSequence([int(k) & 0xFFFFFFFF for k in keys]).generate_state(2, np.uint32)
+    return int((int(st[0]) << 31) ^ int(st[1])) & ((1 << 63) - 1)
 
 
-def round_to(x: np.ndarray, dtype: str) -> torch.Tensor:
+def gen_for(*keys: int) -> torch.Generator:
+    g = torch.Generator()
+    g.manual_seed(seed_for(*keys))
+    return g
+
+
+def uniform(g: torch.Generator, lo: float = 0.0, hi: float = 1.0) -> float:
+    return lo + (hi - lo) * float(torch.rand((), generator=g, dtype=torch.float64))
+
+
+def round_to(x, dtype: str) -> torch.Tensor:
     """Round float data to the storage dtype (round to nearest even)."""
-    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(DTYPES[dtype])
+    if isinstance(x, np.ndarray):
+        x = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return x.to(torch.float32).to(DTYPES[dtype])
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
@@ -61,10 +74,10 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
 
-def zipf_bias(seed: int, V: int) -> np.ndarray:
+def zipf_bias(seed: int, V: int) -> torch.Tensor:
     """-1.1 * ln(rank(x)) with rank = perm(x) + 1, one permutation per seed."""
-    perm = rng_for(seed, 0x7FFFFFFF).permutation(V)
-    return (-1.1 * np.log(perm.astype(np.float64) + 1.0)).astype(np.float32)
+    perm = torch.randperm(V, generator=gen_for(seed, 0x7FFFFFFF)).to(torch.float64)
+    return (-1.1 * torch.log(perm + 1.0)).to(torch.float32)
 
 
 @dataclass
@@ -123,56 +136,54 @@ class TreeCase:
 def make_chain(name: str, seed: int, B: int, gamma: int, V: int, dtype: str = "bf16",
                target: str = "zipf", target_sigma: float = 1.0,
                draft_sigma: tuple = (1.0, 1.0),
-               temperature: Callable[[int, np.random.Generator], float] | float = 1.0,
+               temperature: Callable[[int, float], float] | float = 1.0,
                draft_probs: bool = False, draft_probs_T: float = 1.0,
-               force_accept_every: int = 0) -> ChainCase:
-    """General chain workload; every row b uses the Philox stream (seed, b).
+               force_accept_every: int = 0, row0: int = 0) -> ChainCase:
+    """General chain workload; row b uses the generator (seed, row0 + b), so
+    a batch starting at ``row0`` continues the same row stream.
 
     target: "zipf" -> N(0, target_sigma^2) - 1.1 ln(rank); "normal" ->
     N(0, target_sigma^2).  Draft logits = target (before rounding) + N(0, s_b^2)
     with s_b ~ U[draft_sigma].  ``temperature`` is a constant or a callable
-    (b, rng) -> T.  With ``draft_probs`` the draft is stored as fp32
-    probabilities softmax((target + noise) / draft_probs_T) and the target
-    keeps the row temperature.
+    (b, v) -> T of a per-row uniform v in [0, 1).  With ``draft_probs`` the
+    draft is stored as fp32 probabilities softmax((target + noise) /
+    draft_probs_T) and the target keeps the row temperature.
     """
     bias = zipf_bias(seed, V) if target == "zipf" else None
     tgt = torch.empty((B, gamma + 1, V), dtype=DTYPES[dtype])
     ddt = "f32" if draft_probs else dtype
     dft = torch.empty((B, gamma, V), dtype=DTYPES[ddt])
-    toks = np.empty((B, gamma), np.int32)
-    temps = np.empty(B, np.float32)
-    unif = np.empty((B, gamma + 1), np.float32)
-    for b in range(B):
-        rng = rng_for(seed, b)
-        base = rng.standard_normal((gamma + 1, V), dtype=np.float32) * np.float32(target_sigma)
+    toks = torch.empty((B, gamma), dtype=torch.int32)
+    temps = torch.empty(B, dtype=torch.float32)
+    unif = torch.empty((B, gamma + 1), dtype=torch.float32)
+    for i in range(B):
+        b = row0 + i
+        g = gen_for(seed, b)
+        base = torch.randn((gamma + 1, V), generator=g) * float(target_sigma)
         if bias is not None:
             base += bias
-        s_b = rng.uniform(draft_sigma[0], draft_sigma[1])
-        dl = base[:gamma] + rng.standard_normal((gamma, V), dtype=np.float32) * np.float32(s_b)
-        T = temperature(b, rng) if callable(temperature) else float(temperature)
-        temps[b] = T
-        unif[b] = rng.random(gamma + 1, dtype=np.float32)
+        s_b = uniform(g, draft_sigma[0], draft_sigma[1])
+        dl = base[:gamma] + torch.randn((gamma, V), generator=g) * float(s_b)
+        v = uniform(g)
+        T = float(temperature(b, v)) if callable(temperature) else float(temperature)
+        temps[i] = T
+        unif[i] = torch.rand(gamma + 1, generator=g)
         if force_accept_every and b % force_accept_every == 0:
-            unif[b, :gamma] = 0.0
-        gumbel = rng.gumbel(size=(gamma, V))
-        tgt[b] = round_to(base, dtype)
+            unif[i, :gamma] = 0.0
+        tgt[i] = base.to(DTYPES[dtype])
         if draft_probs:
-            z = dl.astype(np.float64) / draft_probs_T
-            z -= z.max(axis=1, keepdims=True)
-            e = np.exp(z)
-            probs = (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
-            dft[b] = torch.from_numpy(probs)
-            with np.errstate(divide="ignore"):
-                toks[b] = np.argmax(np.log(probs.astype(np.float64)) + gumbel, axis=1)
+            q = torch.softmax(dl / draft_probs_T, dim=-1)
+            dft[i] = q
+            toks[i] = torch.multinomial(q, 1, generator=g)[:, 0].to(torch.int32)
         else:
-            dft[b] = round_to(dl, dtype)
-            dr = to_f64(dft[b])
+            dft[i] = dl.to(DTYPES[dtype])
+            dr = dft[i].to(torch.float32)
             if T <= 0:
-                toks[b] = np.argmax(dr, axis=1)
+                toks[i] = torch.argmax(dr, dim=-1).to(torch.int32)
             else:
-                toks[b] = np.argmax(dr / T + gumbel, axis=1)
-    return ChainCase(name, tgt, dft, draft_probs, torch.from_numpy(toks),
-                     torch.from_numpy(temps), torch.from_numpy(unif),
+                q = torch.softmax(dr / T, dim=-1)
+                toks[i] = torch.multinomial(q, 1, generator=g)[:, 0].to(torch.int32)
+    return ChainCase(name, tgt, dft, draft_probs, toks, temps, unif,
                      dict(seed=seed, dtype=dtype, draft_dtype=ddt))
 
 
@@ -191,9 +202,8 @@ def c2_chain_bf16_v32000(T: float, rounds: int = 4096, seed: int = 1002) -> Chai
                       "bf16", target="zipf", draft_sigma=(1.0, 1.0), temperature=float(T))
 
 
-def _c3_temperature(b: int, rng: np.random.Generator) -> float:
-    T = rng.uniform(0.0, 1.2)
-    return 0.0 if b % 8 == 0 else T
+def _c3_temperature(b: int, v: float) -> float:
+    return 0.0 if b % 8 == 0 else 1.2 * v
 
 
 def c3_chain_bf16_v128256(B: int = 64, gamma: int = 7, V: int = 128256,
@@ -225,7 +235,8 @@ def make_tree(name: str, seed: int, B: int = 16, N: int = 64, V: int = 32000,
     parents = np.empty((B, N), np.int32)
     tokens = np.empty((B, N), np.int32)
     for b in range(B):
-        rng = rng_for(seed, b)
+        rng = np.random.Generator(np.random.SFC64(seed_for(seed, b, 1)))
+        g = gen_for(seed, b)
         par, dep = [-1], [0]
         queue = deque([0])
         while len(par) < N:
@@ -250,16 +261,16 @@ def make_tree(name: str, seed: int, B: int = 16, N: int = 64, V: int = 32000,
         for n in range(N):
             if len(children[n]):
                 tok[children[n]] = rng.choice(V, size=len(children[n]), replace=False)
-        lg = rng.standard_normal((N, V), dtype=np.float32) * np.float32(sigma)
+        lg = torch.randn((N, V), generator=g) * float(sigma)
         cur = 0
         while len(children[cur]):
             c = int(rng.choice(children[cur]))
             if rng.random() < p_match:
-                lg[cur, tok[c]] = lg[cur].max() + 1.0
+                lg[cur, int(tok[c])] = lg[cur].max() + 1.0
             else:
-                lg[cur, tok[c]] = lg[cur].min() - 1.0
+                lg[cur, int(tok[c])] = lg[cur].min() - 1.0
             cur = c
-        logits[b] = round_to(lg, dtype)
+        logits[b] = lg.to(DTYPES[dtype])
         parents[b] = par_a
         tokens[b] = tok
     return TreeCase(name, logits, torch.from_numpy(parents), torch.from_numpy(tokens),
