@@ -25,12 +25,11 @@
  *    The library never allocates and never synchronises the host; work is
  *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *  - `workspace` is caller-owned device memory of at least
- *    spec_verify_workspace_bytes(...) bytes, 16-byte aligned, ZERO-FILLED
- *    before its first use (e.g. cudaMemsetAsync).  Every call that completes
- *    leaves its counter words at zero again, so a workspace can be reused by
- *    later calls in stream order without clearing.  Calls that may overlap on
- *    the GPU need distinct workspaces.  After a row reports SV_ROW_TIMEOUT the
- *    workspace must be zero-filled again before reuse.
+ *    spec_verify_workspace_bytes(...) bytes, 16-byte aligned, with no
+ *    initialisation required: every call first zeroes the workspace's small
+ *    control block (one cudaMemsetAsync on `stream`).  Calls that may overlap
+ *    on the GPU need distinct workspaces; calls in stream order may share one,
+ *    whatever their shapes.
  *  - Row alignment is the caller's job: target row i scores draft i (the
  *    distribution conditioned on the context and drafts 0..i-1); row gamma is
  *    the bonus row.

@@ -90,9 +90,9 @@ def spec_verify_workspace_bytes(B: int, rows_per_batch: int, V: int, dtype: int 
 
 
 # ---------------------------------------------------------------------------
-# Workspace cache: one zero-filled buffer per (device, stream), grown on
-# demand.  The library leaves it zeroed after every call, so it is reused
-# by later calls on the same stream without clearing.
+# Workspace cache: one buffer per (device, stream), grown on demand.  Each
+# library call zeroes the control block it needs, so calls of any shape in
+# stream order can share the buffer.
 # ---------------------------------------------------------------------------
 
 _ws_cache: dict = {}
@@ -104,7 +104,7 @@ def workspace_for(device: torch.device, stream_ptr: int, nbytes: int) -> torch.T
     with _ws_lock:
         ws = _ws_cache.get(key)
         if ws is None or ws.numel() < nbytes:
-            ws = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
+            ws = torch.empty(max(nbytes, 4096), dtype=torch.uint8, device=device)
             _ws_cache[key] = ws
         return ws
 

@@ -38,6 +38,8 @@ static void fill_workspace(KParams &P, void *ws, const Layout &L) {
   P.a_count = reinterpret_cast<unsigned *>(w + L.a_count);
   P.b_count = reinterpret_cast<unsigned *>(w + L.b_count);
   P.flag = reinterpret_cast<unsigned *>(w + L.flag);
+  P.err = reinterpret_cast<int *>(w + L.err);
+  P.ctrl_bytes = L.ctrl;
   P.dec = reinterpret_cast<Decision *>(w + L.dec);
   P.partA = reinterpret_cast<float2 *>(w + L.partA);
   P.partB = reinterpret_cast<float *>(w + L.partB);

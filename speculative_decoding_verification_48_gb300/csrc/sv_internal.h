@@ -28,12 +28,11 @@ enum DecKind { DEC_DONE = 0, DEC_RESIDUAL = 1 };
 struct Decision {
   int kind;    // DecKind
   int j;       // first rejected position
-  int err;     // SV_ROW_TIMEOUT bits set by Phase-B units whose wait ran out
-  int pad0;
+  int pad0, pad1;
   float c;     // log2(e) / T
   float Mp, invZp, Mq, invZq;  // row maxima and 1 / normalisers of rows p_j, q_j
   float u;     // the categorical draw u_gamma
-  float pad1[6];
+  float pad2[6];
 };
 static_assert(sizeof(Decision) == 64, "Decision must stay 64 bytes");
 
@@ -44,9 +43,13 @@ struct WsHeader {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout for B batch rows of `rows` logit rows of V entries.
+// Workspace layout for B batch rows of `rows` logit rows of V entries.  The
+// control block [0, ctrl) holds the work counters, per-row arrival counters,
+// decision flags and error words; every call zeroes it first (one small
+// memset), so a workspace needs no initialisation and may be shared by calls
+// of different shapes in stream order.
 struct Layout {
-  size_t a_count, b_count, flag, dec, partA, partB, total;
+  size_t a_count, b_count, flag, err, ctrl, dec, partA, partB, total;
   int tiles;
 };
 
@@ -57,6 +60,8 @@ inline Layout make_layout(int B, int rows, int V) {
   L.a_count = off; off = align_up(off + (size_t)B * 4, 256);
   L.b_count = off; off = align_up(off + (size_t)B * 4, 256);
   L.flag = off;    off = align_up(off + (size_t)B * 4, 256);
+  L.err = off;     off = align_up(off + (size_t)B * 4, 256);
+  L.ctrl = off;
   L.dec = off;     off = align_up(off + (size_t)B * sizeof(Decision), 256);
   L.partA = off;   off = align_up(off + (size_t)B * rows * L.tiles * sizeof(float2), 256);
   L.partB = off;   off = align_up(off + (size_t)B * L.tiles * sizeof(float), 256);
@@ -88,6 +93,8 @@ struct KParams {
   float *out_diag;
   WsHeader *hdr;
   unsigned *a_count, *b_count, *flag;
+  int *err;                   // per-row SV_ROW_TIMEOUT bits from Phase-B waits
+  size_t ctrl_bytes;          // bytes of the control block zeroed per call
   Decision *dec;
   float2 *partA;
   float *partB;

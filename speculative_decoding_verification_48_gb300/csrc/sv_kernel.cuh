@@ -870,7 +870,7 @@ __device__ void run_unit_B(const KParams &P, int b, int t, SmemChain &sm) {
       sm.dec.invZq = __ldcg(&d->invZq);
       sm.dec.u = __ldcg(&d->u);
     } else {
-      atomicOr(&P.dec[b].err, SV_ROW_TIMEOUT);
+      atomicOr(P.err + b, SV_ROW_TIMEOUT);
     }
   }
   __syncthreads();
@@ -892,7 +892,7 @@ __device__ void run_unit_B(const KParams &P, int b, int t, SmemChain &sm) {
   __syncthreads();
   if (sm.flag2) {
     __threadfence();
-    const int err = __ldcg(&P.dec[b].err);
+    const int err = __ldcg(P.err + b);
     if (err) {
       write_error_row(P, b, err, G1, P.out_tokens + (size_t)b * G1, nullptr);
     } else if (ok && d.kind == DEC_RESIDUAL) {
@@ -900,7 +900,7 @@ __device__ void run_unit_B(const KParams &P, int b, int t, SmemChain &sm) {
     }
     if (threadIdx.x == 0) {
       P.b_count[b] = 0;
-      P.dec[b].err = 0;
+      P.err[b] = 0;
       P.flag[b] = 0;
     }
   }

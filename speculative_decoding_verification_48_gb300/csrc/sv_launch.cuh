@@ -39,6 +39,7 @@ sv_status launch_phase(const KParams &P0, const Sched &s, cudaStream_t stream) {
 template <int MODE, int TDT, int DDT, bool PROBS>
 sv_status launch_verify(const KParams &P, cudaStream_t stream) {
   const int B = P.B, A = P.rows * P.tiles;
+  if (cudaMemsetAsync(P.hdr, 0, P.ctrl_bytes, stream) != cudaSuccess) return SV_ERR_CUDA;
   if constexpr (MODE == MODE_CHAIN) {
     // Phase A (+ decisions), then Phase B (+ finalisation) in stream order.
     const int Bc = P.tiles;

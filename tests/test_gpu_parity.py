@@ -328,7 +328,7 @@ def test_workspace_reuse_across_entry_points(sv):
     tree = W.make_tree("ws", 4301, B=4, N=32, V=17000)
     nb = max(sv.spec_verify_workspace_bytes(8, 9, 17000),
              sv.spec_verify_workspace_bytes(4, 32, 17000))
-    ws = torch.zeros(nb, dtype=torch.uint8, device=DEV)
+    ws = torch.full((nb,), 0xAB, dtype=torch.uint8, device=DEV)   # no initialisation needed
     c_args = [t.to(DEV) for t in (chain.target, chain.draft, chain.draft_tokens,
                                   chain.temperatures, chain.uniforms)]
     t_args = [t.to(DEV) for t in (tree.node_logits, tree.parent, tree.node_tokens)]
