@@ -359,6 +359,16 @@ __device__ __forceinline__ float2 tile_argmax(const typename Elt<DT>::T *row, in
   return make_float2(m, __int_as_float(idx == 0x7fffffff ? idx : x0 + idx));
 }
 
+// max(0, p(x) - q(x)) from the logits (or the given probability q).  Both
+// products are rounded separately (no FMA contraction), so identical target
+// and draft rows give exactly zero.
+template <bool PROBS>
+__device__ __forceinline__ float residual_term(float lp, float lq, const Decision &d) {
+  const float p = __fmul_rn(ex2(__fmul_rn(lp - d.Mp, d.c)), d.invZp);
+  const float q = PROBS ? lq : __fmul_rn(ex2(__fmul_rn(lq - d.Mq, d.c)), d.invZq);
+  return max_nan(0.f, __fsub_rn(p, q));
+}
+
 // Residual tile mass sum_x max(0, p(x) - q(x)) over one tile of the row
 // pair (p_j, q_j); NaN propagates.
 template <int TDT, int DDT, bool PROBS>
@@ -377,11 +387,7 @@ __device__ __forceinline__ float tile_residual(const typename Elt<TDT>::T *prow,
     tp.get(k, a, -CUDART_INF_F);
     tq.get(k, b, PROBS ? 0.f : -CUDART_INF_F);
 #pragma unroll
-    for (int t = 0; t < VEC; ++t) {
-      const float p = ex2((a[t] - d.Mp) * d.c) * d.invZp;
-      const float q = PROBS ? b[t] : ex2((b[t] - d.Mq) * d.c) * d.invZq;
-      s += max_nan(0.f, p - q);
-    }
+    for (int t = 0; t < VEC; ++t) s += residual_term<PROBS>(a[t], b[t], d);
   }
   return block_sum(s, sm);
 }
@@ -702,10 +708,7 @@ __device__ void finalize_residual(const KParams &P, int b, const Decision &d, Sm
     const TT *pt = prow + x0;
     const DTy *qt = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V + x0;
     k = x0 + crossing_scan(n, base, target, [&](int e) {
-          const float p = ex2((Elt<TDT>::load1(pt + e) - d.Mp) * d.c) * d.invZp;
-          const float q = PROBS ? Elt<DDT>::load1(qt + e)
-                                : ex2((Elt<DDT>::load1(qt + e) - d.Mq) * d.c) * d.invZq;
-          return max_nan(0.f, p - q);
+          return residual_term<PROBS>(Elt<TDT>::load1(pt + e), Elt<DDT>::load1(qt + e), d);
         }, sm);
   }
   if (threadIdx.x == 0) {
