@@ -2,8 +2,9 @@
 // parameter packing and dispatch.  Every check that can fail happens before
 // the first CUDA call, so an invalid call touches no GPU state.
 #include <atomic>
+#include <cstdlib>
 
-#include "sv_internal.h"
+#include "sv_stream.cuh"
 
 namespace sv {
 
@@ -18,6 +19,13 @@ int sm_count(int device) {
   return v;
 }
 
+size_t workspace_bytes_any(int B, int rows, int V) {
+  const size_t a = make_layout(B, rows, V).total;
+  // smallest tiles (fp32 rows) give the most partials
+  const size_t b = make_stream_layout(B, rows, V, 4, 4, false).total;
+  return a > b ? a : b;
+}
+
 static bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16 || d == SV_F16; }
 
 static size_t dtype_size(int d) { return d == SV_F32 ? 4 : 2; }
@@ -25,6 +33,16 @@ static size_t dtype_size(int d) { return d == SV_F32 ? 4 : 2; }
 // Natural alignment of a (nullable) pointer.
 static bool aligned_to(const void *p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+// The streaming kernel is used for aligned rows unless SPEC_VERIFY_KERNEL=tile
+// selects the register-tile kernel for every shape (for comparisons).
+static int stream_enabled() {
+  static const int v = [] {
+    const char *e = getenv("SPEC_VERIFY_KERNEL");
+    return (e && e[0] == 't') ? 0 : 1;
+  }();
+  return v;
 }
 
 // Units are counted in 32-bit integers on the device.
@@ -55,7 +73,7 @@ extern "C" {
 SV_API size_t spec_verify_workspace_bytes(int B, int rows_per_batch, int V, sv_dtype dt) {
   (void)dt;
   if (B <= 0 || rows_per_batch <= 0 || V <= 0 || V > SV_MAX_VOCAB) return 0;
-  return make_layout(B, rows_per_batch, V).total;
+  return workspace_bytes_any(B, rows_per_batch, V);
 }
 
 SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt, const void *draft,
@@ -80,7 +98,8 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt, cons
     return SV_ERR_INVALID_ARG;
   const int rows = (gamma + 1) + (probs ? 0 : gamma);
   const Layout L = make_layout(B, rows, V);
-  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15))
+  if (workspace_bytes < workspace_bytes_any(B, rows, V) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15))
     return SV_ERR_INVALID_ARG;
   if (!units_fit(B, (long long)rows * L.tiles)) return SV_ERR_UNSUPPORTED;
 
@@ -95,6 +114,7 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt, cons
   P.V = V;
   P.rows = rows;
   P.phase_b = 1;
+  P.use_stream = stream_enabled();
   P.out_tokens = out_tokens;
   P.out_nacc = out_num_accepted;
   P.out_diag = out_diag;
@@ -125,7 +145,8 @@ SV_API sv_status spec_verify_chain_greedy(const void *target_logits, sv_dtype td
     return SV_ERR_INVALID_ARG;
   const int rows = gamma + 1;
   const Layout L = make_layout(B, rows, V);
-  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15))
+  if (workspace_bytes < workspace_bytes_any(B, rows, V) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15))
     return SV_ERR_INVALID_ARG;
   if (!units_fit(B, (long long)rows * L.tiles)) return SV_ERR_UNSUPPORTED;
 
@@ -137,6 +158,7 @@ SV_API sv_status spec_verify_chain_greedy(const void *target_logits, sv_dtype td
   P.V = V;
   P.rows = rows;
   P.phase_b = 0;
+  P.use_stream = stream_enabled();
   P.out_tokens = out_tokens;
   P.out_nacc = out_num_accepted;
   P.out_status = out_row_status;
@@ -162,7 +184,8 @@ SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
       !aligned_to(out_num_accepted, 4) || !aligned_to(out_row_status, 4))
     return SV_ERR_INVALID_ARG;
   const Layout L = make_layout(B, N, V);
-  if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15))
+  if (workspace_bytes < workspace_bytes_any(B, N, V) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15))
     return SV_ERR_INVALID_ARG;
   if (!units_fit(B, (long long)N * L.tiles)) return SV_ERR_UNSUPPORTED;
 
@@ -176,6 +199,7 @@ SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
   P.rows = N;
   P.max_depth = max_depth;
   P.phase_b = 0;
+  P.use_stream = stream_enabled();
   P.out_path = out_path;
   P.out_tokens = out_tokens;
   P.out_nacc = out_num_accepted;

@@ -89,6 +89,7 @@ struct KParams {
   const int32_t *node_tokens;
   int B, gamma, V, tiles, rows, N, max_depth;
   int phase_b;                // 1 if the call has Phase-B units (publish decisions)
+  int use_stream;             // allow the streaming (TMA ring) kernel
   int32_t *out_tokens, *out_nacc, *out_status, *out_path;
   float *out_diag;
   WsHeader *hdr;
@@ -111,5 +112,8 @@ sv_status launch_tree(const KParams &P, sv_dtype dt, cudaStream_t stream);
 
 // Device properties cached per device (host side).
 int sm_count(int device);
+
+// Workspace bytes covering both kernel families for the given shape.
+size_t workspace_bytes_any(int B, int rows, int V);
 
 }  // namespace sv

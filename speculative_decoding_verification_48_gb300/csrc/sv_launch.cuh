@@ -3,7 +3,7 @@
 
 #include <atomic>
 
-#include "sv_kernel.cuh"
+#include "sv_stream.cuh"
 
 namespace sv {
 
@@ -36,8 +36,85 @@ sv_status launch_phase(const KParams &P0, const Sched &s, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+// Streaming kernel: one persistent CTA per SM.
+template <int MODE, int TDT, int DDT, bool PROBS>
+sv_status launch_stream(const KParams &P0, cudaStream_t stream) {
+  auto kern = sv_stream_kernel<MODE, TDT, DDT, PROBS>;
+  static std::atomic<int> attr_done[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
+  if (!attr_done[dev].load(std::memory_order_relaxed)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStreamSmemBytes) != cudaSuccess)
+      return SV_ERR_CUDA;
+    attr_done[dev].store(1, std::memory_order_relaxed);
+  }
+  const int sms = sm_count(dev);
+  if (sms <= 0) return SV_ERR_CUDA;
+  const int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
+  const StreamLayout L = make_stream_layout(P0.B, P0.rows, P0.V, esT, esD, PROBS);
+  char *w = reinterpret_cast<char *>(P0.hdr);
+  SParams S{};
+  S.target = P0.target;
+  S.draft = P0.draft;
+  S.draft_tokens = P0.draft_tokens;
+  S.temps = P0.temps;
+  S.unif = P0.unif;
+  S.parent = P0.parent;
+  S.node_tokens = P0.node_tokens;
+  S.B = P0.B;
+  S.gamma = P0.gamma;
+  S.V = P0.V;
+  S.N = P0.N;
+  S.max_depth = P0.max_depth;
+  S.rows = P0.rows;
+  S.tilesT = L.tilesT;
+  S.tilesD = L.tilesD;
+  S.tilesMax = L.tilesMax;
+  S.tilesB = L.tilesB;
+  S.TA_T = L.TA_T;
+  S.TA_D = L.TA_D;
+  S.TB = L.TB;
+  if (MODE == MODE_CHAIN) {
+    const int G1 = P0.gamma + 1;
+    S.unitsA = G1 * L.tilesT + (PROBS ? 0 : P0.gamma * L.tilesD);
+  } else {
+    S.unitsA = P0.rows * L.tilesT;
+  }
+  S.totalA = P0.B * S.unitsA;
+  S.out_tokens = P0.out_tokens;
+  S.out_nacc = P0.out_nacc;
+  S.out_status = P0.out_status;
+  S.out_path = P0.out_path;
+  S.out_diag = P0.out_diag;
+  S.hdr = reinterpret_cast<StreamHeader *>(w);
+  S.a_count = reinterpret_cast<unsigned *>(w + L.a_count);
+  S.b_count = reinterpret_cast<unsigned *>(w + L.b_count);
+  S.row_done = reinterpret_cast<unsigned *>(w + L.row_done);
+  S.qitems = reinterpret_cast<unsigned *>(w + L.qitems);
+  S.dec = reinterpret_cast<Decision *>(w + L.dec);
+  S.partA = reinterpret_cast<float2 *>(w + L.partA);
+  S.partB = reinterpret_cast<float *>(w + L.partB);
+  if (cudaMemsetAsync(w, 0, L.ctrl, stream) != cudaSuccess) return SV_ERR_CUDA;
+  kern<<<sms, kStreamThreads, kStreamSmemBytes, stream>>>(S);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+// Rows of both logit arrays start on 16-byte boundaries.
+inline bool rows_aligned(const void *p, int V, int es) {
+  return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0 && ((size_t)V * es) % 16 == 0;
+}
+
 template <int MODE, int TDT, int DDT, bool PROBS>
 sv_status launch_verify(const KParams &P, cudaStream_t stream) {
+  {
+    const int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
+    bool ok = rows_aligned(P.target, P.V, esT);
+    if (MODE == MODE_CHAIN) ok = ok && rows_aligned(P.draft, P.V, esD);
+    // Phase-B queue items pack b * tilesB + t in 27 bits
+    if (MODE == MODE_CHAIN) ok = ok && (long long)P.B * ((P.V + 4095) / 4096) < (1LL << 26);
+    if (ok && P.use_stream) return launch_stream<MODE, TDT, DDT, PROBS>(P, stream);
+  }
   const int B = P.B, A = P.rows * P.tiles;
   if (cudaMemsetAsync(P.hdr, 0, P.ctrl_bytes, stream) != cudaSuccess) return SV_ERR_CUDA;
   if constexpr (MODE == MODE_CHAIN) {
