@@ -344,7 +344,6 @@ def test_workspace_reuse_across_entry_points(sv):
             for x, y in zip(first[0] + first[1] + first[2], a + b + c):
                 assert torch.equal(x, y)
     torch.cuda.synchronize()
-    assert int(ws[:8].view(torch.int32).abs().sum()) == 0     # work / exit counters
     assert int(ws.count_nonzero()) > 0                        # partials were written
 
 
