@@ -95,6 +95,8 @@ sv_status launch_stream(const KParams &P0, cudaStream_t stream) {
   S.dec = reinterpret_cast<Decision *>(w + L.dec);
   S.partA = reinterpret_cast<float2 *>(w + L.partA);
   S.partB = reinterpret_cast<float *>(w + L.partB);
+  S.partT = reinterpret_cast<float2 *>(w + L.partT);
+  S.partBT = reinterpret_cast<float *>(w + L.partBT);
   if (cudaMemsetAsync(w, 0, L.ctrl, stream) != cudaSuccess) return SV_ERR_CUDA;
   kern<<<sms, kStreamThreads, kStreamSmemBytes, stream>>>(S);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
