@@ -32,129 +32,136 @@
 
 namespace sv {
 
-// Scheduler (one thread of its own warp): decides the unit sequence and
-// writes one descriptor per unit into a shared-memory ring.  All global
-// round trips of scheduling (Phase-A claims, temperatures, Phase-B tickets
-// and decision records) happen here, off the thread that arrives on the
-// stage barriers, and none of their results is needed in the iteration that
-// requests it.  Phase-A claims take batches of up to kClaim consecutive
-// units while many remain (single units near the end); a batch is decoded
-// once and then walked with increments.
+// Scheduler (a whole warp): decides the unit sequence and writes one
+// descriptor per unit into a shared-memory ring, up to kSchedBatch units per
+// step with one lane per unit, published with one fence per step.  It owns
+// every global round trip of scheduling, so the producer's stage-barrier
+// arrivals never wait on loads.
+//   Phase B: the device-wide queue is split round-robin, CTA c owning slots
+//   c, c + G, c + 2G, ...; lanes poll the next owned slots together and the
+//   published prefix becomes descriptors (decision record loaded per lane).
+//   Phase A: claims of up to kClaim consecutive units from a device-wide
+//   counter while many remain (single units near the end), two claims in
+//   flight so a batch's temperatures are requested a batch ahead.
 template <int MODE, int TDT, int DDT, bool PROBS>
 __device__ void stream_scheduler(const SParams &P, StreamSmem &sm) {
+  const int lane = lane_id();
   const int G1 = P.gamma + 1;
   const unsigned totalA = (unsigned)P.totalA;
-  const unsigned qcap = (unsigned)(P.B * P.tilesB);
+  const long long qcap = (long long)P.B * P.tilesB;
   const unsigned grid = gridDim.x;
   const unsigned unitsA = (unsigned)P.unitsA;
   const unsigned kmax = (unsigned)min(kClaim, P.unitsA);
-  const int rowsA = (MODE == MODE_CHAIN) ? (PROBS ? G1 : G1 + P.gamma) : P.rows;
-  auto claim_size = [&](unsigned at) { return (at + 4u * kmax * grid < totalA) ? kmax : 1u; };
-  // Two claims in flight: n1 (next batch, temperatures being fetched) and
-  // n2 (its atomic still returning).
-  unsigned n1_s = atomicAdd(&P.hdr->a_next, kmax), n1_k = kmax;
-  unsigned n2_s = atomicAdd(&P.hdr->a_next, kmax), n2_k = kmax;
+  // claim size shrinks with the work left per CTA: about half of each CTA's
+  // remaining share, between 1 and kmax units
+  auto claim_size = [&](unsigned at) {
+    const unsigned left = at < totalA ? totalA - at : 0u;
+    return max(1u, min(kmax, left / (2u * grid)));
+  };
+  // claims: lane 0 issues, every lane keeps the values (broadcast on use)
+  unsigned n1_s = 0, n1_k = kmax, n2_s = 0, n2_k = kmax;
+  if (lane == 0) {
+    n1_s = atomicAdd(&P.hdr->a_next, kmax);
+    n2_s = atomicAdd(&P.hdr->a_next, kmax);
+  }
+  n1_s = __shfl_sync(0xffffffffu, n1_s, 0);
   float n1_lo = 0.f, n1_hi = 0.f;
   if (MODE == MODE_CHAIN && n1_s < totalA) {
     n1_lo = __ldg(P.temps + n1_s / unitsA);
     n1_hi = __ldg(P.temps + (min(n1_s + n1_k, totalA) - 1u) / unitsA);
   }
-  // current batch: remaining count and the walking position (b, row, tile)
-  unsigned left = 0;
-  int cb = 0, crow = 0, ctile = 0, blo = -1;
+  unsigned cur = 0, cur_end = 0;  // current Phase-A batch
   float Tlo = 0.f, Thi = 0.f;
-  // queue counters in use / loads in flight, pending ticket and its item
-  unsigned qh = 0, qr = 0, qh_n = 0, qr_n = 0;
-  long long ticket = -1;
-  unsigned tw_seen = 0, tw_n = 0;
-  bool tw_fresh = false;
-  bool timed_out = false;
-  for (int it = 0;; ++it) {
+  unsigned blo = 0;
+  long long bnext = blockIdx.x;   // next owned Phase-B queue slot
+  int tail = 0;                   // descriptors written
+  bool stop = false, timed_out = false;
+  long long t0 = clock64();
+  while (!stop) {
+    // room for a full step in the ring
     const long long tw = clock64();
-    while (it - sm.ring_head >= kRing) {
+    while (tail + kSchedBatch - sm.ring_head > kRing) {
       if (clock64() - tw > kStreamWait) { timed_out = true; break; }
     }
-    StageMeta &mt = sm.ring[it % kRing];
-    int kind = U_STOP;
-    const bool poll = (it % kPoll) == 0;
-    const long long t0 = clock64();
-    while (!timed_out) {
-      if constexpr (MODE == MODE_CHAIN) {
-        // Phase-B tiles first: they are L2-hot and unblock finalisation.
-        if (poll || left == 0) {
-          if (ticket < 0 && qh < qr) {
-            ticket = atomicAdd(&P.hdr->q_head, 1u);
-            if (ticket >= (long long)qcap) ticket = -1;  // can never be published
-            qh = qr;
-            tw_seen = 0;
-            tw_fresh = false;
-          } else if (ticket >= 0 && tw_seen == 0) {
-            {
-              // use the value loaded at the previous poll; start the next load
-              if (tw_fresh) tw_seen = tw_n;
-              tw_n = ld_relaxed_u32(P.qitems + ticket);
-              tw_fresh = true;
-            }
-          }
-        }
-        if (ticket >= 0 && tw_seen != 0) {
-          fence_acq_rel_gpu();  // acquire: the decision record published before the item
-          const unsigned v = tw_seen - 1u;
-          ticket = -1;
-          tw_seen = 0;
-          tw_fresh = false;
+    if (timed_out) break;
+    int written = 0;
+    // ---- Phase B: published prefix of the next owned slots
+    if constexpr (MODE == MODE_CHAIN) {
+      const long long slot = bnext + (long long)lane * grid;
+      unsigned w = 0;
+      if (lane < kSchedBatch && slot < qcap) w = ld_relaxed_u32(P.qitems + slot);
+      const unsigned pub = __ballot_sync(0xffffffffu, w != 0);
+      const int nb = __ffs(~pub) - 1;  // leading published slots
+      if (nb > 0) {
+        fence_acq_rel_gpu();  // acquire: decision records published before the items
+        if (lane < nb) {
+          const unsigned v = w - 1u;
           const int j = (int)(v & 31u), bt = (int)(v >> 5);
           const int bb = bt / P.tilesB, tt = bt % P.tilesB;
-          if (bb >= P.B || j >= P.gamma) {
-            // a malformed item: never copy from it
-            atomicOr(&P.hdr->error, 2u);
-            continue;
+          StageMeta &mt = sm.ring[(tail + lane) % kRing];
+          if (bb < P.B && j < P.gamma) {
+            const Decision *d = P.dec + bb;
+            mt.c = __ldcg(&d->c);
+            mt.Mp = __ldcg(&d->Mp);
+            mt.invZp = __ldcg(&d->invZp);
+            mt.Mq = __ldcg(&d->Mq);
+            mt.invZq = __ldcg(&d->invZq);
+            mt.j = j;
+            mt.b = bb;
+            mt.row = 0;
+            mt.tile = tt;
+            mt.isdraft = 0;
+            mt.n = min(P.TB, P.V - tt * P.TB);
+            mt.kind = U_RESID;
+          } else {
+            atomicOr(&P.hdr->error, 2u);  // a malformed item: never copy from it
+            mt.kind = U_SKIP;
+            mt.b = 0;
           }
-          const Decision *d = P.dec + bb;
-          mt.c = __ldcg(&d->c);
-          mt.Mp = __ldcg(&d->Mp);
-          mt.invZp = __ldcg(&d->invZp);
-          mt.Mq = __ldcg(&d->Mq);
-          mt.invZq = __ldcg(&d->invZq);
-          mt.j = j;
-          mt.b = bb;
-          mt.row = 0;
-          mt.tile = tt;
-          mt.isdraft = 0;
-          mt.n = min(P.TB, P.V - tt * P.TB);
-          kind = U_RESID;
-          break;
+        }
+        written = nb;
+        bnext += (long long)nb * grid;
+      }
+    }
+    // ---- Phase A: the rest of the step from the current batch
+    int na = 0;
+    if (written < kSchedBatch) {
+      if (cur >= cur_end) {
+        n1_s = __shfl_sync(0xffffffffu, n1_s, 0);
+        if (n1_s < totalA) {
+          // promote n1; n2 becomes n1 (fetch its temperatures); claim a new n2
+          cur = n1_s;
+          cur_end = min(n1_s + n1_k, totalA);
+          blo = cur / unitsA;
+          Tlo = n1_lo;
+          Thi = n1_hi;
+          n1_s = __shfl_sync(0xffffffffu, n2_s, 0);
+          n1_k = __shfl_sync(0xffffffffu, n2_k, 0);
+          if (MODE == MODE_CHAIN && n1_s < totalA) {
+            n1_lo = __ldg(P.temps + n1_s / unitsA);
+            n1_hi = __ldg(P.temps + (min(n1_s + n1_k, totalA) - 1u) / unitsA);
+          }
+          if (lane == 0) {
+            n2_k = claim_size(max(cur_end, n1_s + n1_k));
+            n2_s = atomicAdd(&P.hdr->a_next, n2_k);
+          }
         }
       }
-      if (left == 0 && n1_s < totalA) {
-        // promote n1 (decode its first unit once); n2 becomes n1; claim n2
-        const unsigned s0 = n1_s;
-        left = min(n1_s + n1_k, totalA) - s0;
-        cb = (int)(s0 / unitsA);
-        const int ri = (int)(s0 % unitsA);
+      na = (int)min((unsigned)(kSchedBatch - written), cur_end - cur);
+      if (lane < na) {
+        const unsigned ua = cur + lane;
+        const int bb = (int)(ua / unitsA), ri = (int)(ua % unitsA);
+        int row, tile, isdraft = 0;
         if (MODE != MODE_CHAIN || ri < G1 * P.tilesT) {
-          crow = ri / P.tilesT;
-          ctile = ri % P.tilesT;
+          row = ri / P.tilesT;
+          tile = ri % P.tilesT;
         } else {
           const int rd = ri - G1 * P.tilesT;
-          crow = G1 + rd / P.tilesD;
-          ctile = rd % P.tilesD;
+          row = G1 + rd / P.tilesD;
+          tile = rd % P.tilesD;
+          isdraft = 1;
         }
-        blo = cb;
-        Tlo = n1_lo;
-        Thi = n1_hi;
-        n1_s = n2_s;
-        n1_k = n2_k;
-        if (MODE == MODE_CHAIN && n1_s < totalA) {
-          n1_lo = __ldg(P.temps + n1_s / unitsA);
-          n1_hi = __ldg(P.temps + (min(n1_s + n1_k, totalA) - 1u) / unitsA);
-        }
-        n2_k = claim_size(max(s0 + left, n1_s + n1_k));
-        n2_s = atomicAdd(&P.hdr->a_next, n2_k);
-      }
-      if (left > 0) {
-        const int isdraft = (MODE == MODE_CHAIN && crow >= G1) ? 1 : 0;
-        const float T = (cb == blo) ? Tlo : Thi;
+        const float T = ((unsigned)bb == blo) ? Tlo : Thi;
         int k = U_ARGMAX;
         float c = 0.f;
         if constexpr (MODE == MODE_CHAIN) {
@@ -162,55 +169,57 @@ __device__ void stream_scheduler(const SParams &P, StreamSmem &sm) {
           else if (T > 0.f) { k = U_SOFTMAX; c = kLog2e / T; }
         }
         const int TA = isdraft ? P.TA_D : P.TA_T;
-        mt.b = cb;
-        mt.row = crow;
-        mt.tile = ctile;
+        StageMeta &mt = sm.ring[(tail + written + lane) % kRing];
+        mt.kind = k;
+        mt.b = bb;
+        mt.row = row;
+        mt.tile = tile;
         mt.isdraft = isdraft;
         mt.c = c;
-        mt.n = min(TA, P.V - ctile * TA);
-        kind = k;
-        // advance (tile, row, batch row)
-        --left;
-        if (++ctile == (isdraft ? P.tilesD : P.tilesT)) {
-          ctile = 0;
-          if (++crow == rowsA) { crow = 0; ++cb; }
-        }
-        break;
+        mt.n = min(TA, P.V - tile * TA);
       }
-      // Phase A exhausted: wait for queued Phase-B tiles or the end.
-      if (MODE != MODE_CHAIN) break;
-      const unsigned dd = ld_acquire(&P.hdr->decisions_done);
-      qh = ld_volatile_u32(&P.hdr->q_head);
-      qr = ld_volatile_u32(&P.hdr->q_reserved);
-      if (ticket >= 0 && ticket < (long long)qcap) {
-        tw_seen = ld_relaxed_u32(P.qitems + ticket);
-        if (tw_seen != 0) continue;
-        // every row decided and the ticket beyond the final count: nothing
-        // will ever be published there
-        if (dd >= (unsigned)P.B && ticket >= (long long)qr) ticket = -1;
+      cur += (unsigned)na;
+      written += na;
+    }
+    if (written == 0) {
+      // nothing to hand out: the end of Phase A
+      if (MODE != MODE_CHAIN) {
+        stop = true;
       } else {
-        if (qh < qr) continue;
-        if (dd >= (unsigned)P.B) break;
+        unsigned dd = 0, qr = 0;
+        if (lane == 0) {
+          dd = ld_acquire(&P.hdr->decisions_done);
+          qr = ld_volatile_u32(&P.hdr->q_reserved);
+        }
+        dd = __shfl_sync(0xffffffffu, dd, 0);
+        qr = __shfl_sync(0xffffffffu, qr, 0);
+        // every row decided and every owned slot below the final count taken
+        if (dd >= (unsigned)P.B && bnext >= (long long)qr) stop = true;
+        else {
+          __nanosleep(200);
+          if (clock64() - t0 > kStreamWait) { timed_out = true; break; }
+        }
       }
-      __nanosleep(200);
-      if (clock64() - t0 > kStreamWait) { timed_out = true; break; }
-    }
-    if (timed_out) kind = U_STOP;
-    mt.kind = kind;
-    __threadfence_block();
-    sm.ring_tail = it + 1;
-    if (kind == U_STOP) break;
-    if constexpr (MODE == MODE_CHAIN) {
-      if (poll) {
-        // use the counters loaded at the previous poll; start the next loads
-        qh = qh_n;
-        qr = qr_n;
-        qh_n = ld_volatile_u32(&P.hdr->q_head);
-        qr_n = ld_volatile_u32(&P.hdr->q_reserved);
+      if (stop) {
+        if (lane == 0) sm.ring[tail % kRing].kind = U_STOP;
+        written = 1;
       }
     }
+    __syncwarp();
+    if (written > 0 && lane == 0) {
+      __threadfence_block();
+      sm.ring_tail = tail + written;
+    }
+    tail += written;
+    if (written > 0) t0 = clock64();  // the end-phase bound counts idle time only
   }
-  if (timed_out) {
+  if (timed_out && lane == 0) {
+    // hand the producer a STOP so the consumers finish
+    const long long tw = clock64();
+    while (tail + 1 - sm.ring_head > kRing && clock64() - tw < kStreamWait) {}
+    sm.ring[tail % kRing].kind = U_STOP;
+    __threadfence_block();
+    sm.ring_tail = tail + 1;
     atomicOr(&P.hdr->error, 1u);
     for (int b = 0; b < P.B; ++b)
       if (ld_volatile_u32(P.row_done + b) == 0 && P.out_status) P.out_status[b] = SV_ROW_TIMEOUT;
@@ -241,6 +250,7 @@ __device__ void stream_producer(const SParams &P, StreamSmem &sm, unsigned char 
     if (timed_out) {
       mt.kind = U_STOP;
     } else {
+      __threadfence_block();  // acquire: the slot was written before the tail
       const volatile StageMeta &d = sm.ring[it % kRing];
       mt.kind = d.kind; mt.b = d.b; mt.row = d.row; mt.tile = d.tile; mt.n = d.n;
       mt.isdraft = d.isdraft; mt.j = d.j; mt.c = d.c; mt.Mp = d.Mp; mt.invZp = d.invZp;
@@ -263,9 +273,10 @@ __device__ void stream_producer(const SParams &P, StreamSmem &sm, unsigned char 
       } else {
         ok = true;
       }
+      if (mt.kind == U_SKIP) ok = true;
       if (!ok) {
         atomicOr(&P.hdr->error, 4u);
-        mt.kind = U_NOOP;
+        mt.kind = U_SKIP;
       }
     }
     if (mt.kind == U_SOFTMAX || mt.kind == U_ARGMAX) {
@@ -362,7 +373,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) sv_stream_kernel(const SPar
 
   if (warp == 3) {
     // ------------------------------------------------------------ scheduler
-    if (lane == 0) stream_scheduler<MODE, TDT, DDT, PROBS>(P, sm);
+    stream_scheduler<MODE, TDT, DDT, PROBS>(P, sm);
     return;
   }
 
@@ -446,7 +457,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) sv_stream_kernel(const SPar
           const float2 tp = merge_slices(U_RESID, wp, 0.f);
           if (lane == 0) P.partBT[ro] = tp.x;
         }
-        if (mt.kind == U_RESID) {
+        if (mt.kind == U_SKIP) {
+          cnt[k] = nullptr;
+          target[k] = 0;
+          item[k] = 0;
+        } else if (mt.kind == U_RESID) {
           cnt[k] = P.b_count + mt.b;
           target[k] = (unsigned)P.tilesB;
           item[k] = D_FINAL;
@@ -460,12 +475,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) sv_stream_kernel(const SPar
       if (lane == 0) {
         fence_acq_rel_gpu();  // the partials above before the arrivals below
         unsigned prev[kBookBatch];
-        for (int k = 0; k < used; ++k) prev[k] = atomicAdd(cnt[k], 1u);
+        for (int k = 0; k < used; ++k) prev[k] = cnt[k] ? atomicAdd(cnt[k], 1u) : 0xffffffffu;
         bool any_last = false;
-        for (int k = 0; k < used; ++k) any_last |= (prev[k] == target[k] - 1);
+        for (int k = 0; k < used; ++k) any_last |= cnt[k] && (prev[k] == target[k] - 1);
         if (any_last) fence_acq_rel_gpu();  // acquire: other CTAs' partials of the row
         for (int k = 0; k < used; ++k) {
-          if (prev[k] == target[k] - 1) {
+          if (cnt[k] && prev[k] == target[k] - 1) {
             const long long tq = clock64();
             while (sm.dq_push - sm.dq_pop >= kDQ && clock64() - tq < kStreamWait) __nanosleep(64);
             reinterpret_cast<volatile int *>(sm.dq)[sm.dq_push % kDQ] = (item[k] << 28) | mts[k].b;

@@ -16,7 +16,8 @@ constexpr int kDQ = 64;                            // decider queue entries
 constexpr int kBookBatch = 4;                      // stages per bookkeeper fence
 constexpr int kClaim = 8;                          // Phase-A units per claim
 constexpr int kPoll = 8;                           // units between queue-counter polls
-constexpr int kRing = 8;                           // scheduler -> producer descriptors
+constexpr int kRing = 16;                          // scheduler -> producer descriptors
+constexpr int kSchedBatch = 8;                     // descriptors per scheduler step
 constexpr long long kStreamWait = 4000000000LL;    // bound of every wait, in clocks
 
 // Elements per Phase-A tile (one row) and per Phase-B tile (a row pair).
@@ -32,7 +33,9 @@ template <int TDT, int DDT> struct TileB {
   static constexpr int kVec = Elt<TDT>::kVec < Elt<DDT>::kVec ? Elt<TDT>::kVec : Elt<DDT>::kVec;
 };
 
-enum UnitKind { U_STOP = 0, U_NOOP = 1, U_SOFTMAX = 2, U_ARGMAX = 3, U_RESID = 4 };
+// U_NOOP units count toward their row (e.g. draft rows of a greedy row);
+// U_SKIP units (rejected descriptors) count toward nothing.
+enum UnitKind { U_STOP = 0, U_NOOP = 1, U_SOFTMAX = 2, U_ARGMAX = 3, U_RESID = 4, U_SKIP = 5 };
 enum DecItem { D_CHAIN = 1, D_FINAL = 2, D_TREE = 3 };
 
 struct StreamHeader {
