@@ -11,12 +11,14 @@
 //                       unit's tile(s) into a ring stage (full barrier);
 //   warps 4..19 consumers  each reduces its 1/16 slice of a stage to a warp
 //                       partial — softmax (max, sum exp2), argmax (max, first
-//                       index) or residual mass — and arrives on done;
-//   warp 1  bookkeeper  releases finished stages (empty barrier), stores the
-//                       slice partials and their merged tile partial, and
-//                       counts the units into their batch rows, one fence per
-//                       batch of stages; the unit that completes a row queues
-//                       the row for the decider;
+//                       index) or residual mass — releases the stage (empty
+//                       barrier) and puts the partial in a shared-memory
+//                       partial ring;
+//   warp 1  bookkeeper  drains the partial ring: stores the slice partials
+//                       and their merged tile partial, and counts the units
+//                       into their batch rows, one fence per batch of units;
+//                       the unit that completes a row queues the row for the
+//                       decider;
 //   warp 2  decider     merges the row's tile partials (one lane per row),
 //                       runs the accept tests / greedy match / tree walk,
 //                       draws the bonus token, or queues the row's Phase-B
@@ -57,6 +59,14 @@ __device__ void stream_scheduler(const SParams &P, StreamSmem &sm) {
   auto claim_size = [&](unsigned at) {
     const unsigned left = at < totalA ? totalA - at : 0u;
     return max(1u, min(kmax, left / (2u * grid)));
+  };
+  // Phase-A units a row reads: all of them for a sampled row, the target
+  // rows' tiles for a greedy row, one no-op unit for an invalid temperature
+  const unsigned tgt_units = (unsigned)(G1 * P.tilesT);
+  auto row_units = [&](float T) -> unsigned {
+    if (MODE != MODE_CHAIN) return unitsA;
+    if (bad_temperature(T)) return 1u;
+    return T > 0.f ? unitsA : tgt_units;
   };
   // claims: lane 0 issues, every lane keeps the values (broadcast on use)
   unsigned n1_s = 0, n1_k = kmax, n2_s = 0, n2_k = kmax;
@@ -99,6 +109,7 @@ __device__ void stream_scheduler(const SParams &P, StreamSmem &sm) {
           const int j = (int)(v & 31u), bt = (int)(v >> 5);
           const int bb = bt / P.tilesB, tt = bt % P.tilesB;
           StageMeta &mt = sm.ring[(tail + lane) % kRing];
+          mt.target = 0;
           if (bb < P.B && j < P.gamma) {
             const Decision *d = P.dec + bb;
             mt.c = __ldcg(&d->c);
@@ -123,34 +134,53 @@ __device__ void stream_scheduler(const SParams &P, StreamSmem &sm) {
         bnext += (long long)nb * grid;
       }
     }
-    // ---- Phase A: the rest of the step from the current batch
-    int na = 0;
-    if (written < kSchedBatch) {
+    // ---- Phase A: the rest of the step from the current batch.  Units a
+    // row does not read are not emitted: a greedy row reads only its target
+    // rows, a row with an invalid temperature reads nothing and gets one
+    // no-op unit; every emitted unit carries its row's unit count.
+    bool moved = written > 0, promoted = false;
+    while (written < kSchedBatch) {
       if (cur >= cur_end) {
+        // a second promotion in one step would wait on the claim and the
+        // temperature loads just issued: publish what the step has first
+        if (promoted && written > 0) break;
         n1_s = __shfl_sync(0xffffffffu, n1_s, 0);
-        if (n1_s < totalA) {
-          // promote n1; n2 becomes n1 (fetch its temperatures); claim a new n2
-          cur = n1_s;
-          cur_end = min(n1_s + n1_k, totalA);
-          blo = cur / unitsA;
-          Tlo = n1_lo;
-          Thi = n1_hi;
-          n1_s = __shfl_sync(0xffffffffu, n2_s, 0);
-          n1_k = __shfl_sync(0xffffffffu, n2_k, 0);
-          if (MODE == MODE_CHAIN && n1_s < totalA) {
-            n1_lo = __ldg(P.temps + n1_s / unitsA);
-            n1_hi = __ldg(P.temps + (min(n1_s + n1_k, totalA) - 1u) / unitsA);
-          }
-          if (lane == 0) {
-            n2_k = claim_size(max(cur_end, n1_s + n1_k));
-            n2_s = atomicAdd(&P.hdr->a_next, n2_k);
-          }
+        if (n1_s >= totalA) break;
+        promoted = true;
+        // promote n1; n2 becomes n1 (fetch its temperatures); claim a new n2
+        cur = n1_s;
+        cur_end = min(n1_s + n1_k, totalA);
+        blo = cur / unitsA;
+        Tlo = n1_lo;
+        Thi = n1_hi;
+        n1_s = __shfl_sync(0xffffffffu, n2_s, 0);
+        n1_k = __shfl_sync(0xffffffffu, n2_k, 0);
+        if (MODE == MODE_CHAIN && n1_s < totalA) {
+          n1_lo = __ldg(P.temps + n1_s / unitsA);
+          n1_hi = __ldg(P.temps + (min(n1_s + n1_k, totalA) - 1u) / unitsA);
+        }
+        if (lane == 0) {
+          n2_k = claim_size(max(cur_end, n1_s + n1_k));
+          n2_s = atomicAdd(&P.hdr->a_next, n2_k);
         }
       }
-      na = (int)min((unsigned)(kSchedBatch - written), cur_end - cur);
-      if (lane < na) {
-        const unsigned ua = cur + lane;
-        const int bb = (int)(ua / unitsA), ri = (int)(ua % unitsA);
+      moved = true;
+      {
+        // jump over the unread tail of the row at cur (warp-uniform)
+        const unsigned bb = cur / unitsA, ri = cur % unitsA;
+        if (ri >= row_units(bb == blo ? Tlo : Thi)) {
+          cur = min(cur_end, (bb + 1u) * unitsA);
+          continue;
+        }
+      }
+      const int na = (int)min((unsigned)(kSchedBatch - written), cur_end - cur);
+      const unsigned ua = cur + (unsigned)lane;
+      const int bb = (int)(ua / unitsA), ri = (int)(ua % unitsA);
+      const float T = ((unsigned)bb == blo) ? Tlo : Thi;
+      const unsigned target = row_units(T);
+      const bool keep = lane < na && (unsigned)ri < target;
+      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      if (keep) {
         int row, tile, isdraft = 0;
         if (MODE != MODE_CHAIN || ri < G1 * P.tilesT) {
           row = ri / P.tilesT;
@@ -161,15 +191,15 @@ __device__ void stream_scheduler(const SParams &P, StreamSmem &sm) {
           tile = rd % P.tilesD;
           isdraft = 1;
         }
-        const float T = ((unsigned)bb == blo) ? Tlo : Thi;
         int k = U_ARGMAX;
         float c = 0.f;
         if constexpr (MODE == MODE_CHAIN) {
-          if (bad_temperature(T) || (isdraft && T <= 0.f)) k = U_NOOP;
+          if (bad_temperature(T)) k = U_NOOP;
           else if (T > 0.f) { k = U_SOFTMAX; c = kLog2e / T; }
         }
         const int TA = isdraft ? P.TA_D : P.TA_T;
-        StageMeta &mt = sm.ring[(tail + written + lane) % kRing];
+        const int pos = __popc(km & ((1u << lane) - 1u));
+        StageMeta &mt = sm.ring[(tail + written + pos) % kRing];
         mt.kind = k;
         mt.b = bb;
         mt.row = row;
@@ -177,11 +207,12 @@ __device__ void stream_scheduler(const SParams &P, StreamSmem &sm) {
         mt.isdraft = isdraft;
         mt.c = c;
         mt.n = min(TA, P.V - tile * TA);
+        mt.target = (int)target;
       }
       cur += (unsigned)na;
-      written += na;
+      written += __popc(km);
     }
-    if (written == 0) {
+    if (!moved) {
       // nothing to hand out: the end of Phase A
       if (MODE != MODE_CHAIN) {
         stop = true;
@@ -211,7 +242,7 @@ __device__ void stream_scheduler(const SParams &P, StreamSmem &sm) {
       sm.ring_tail = tail + written;
     }
     tail += written;
-    if (written > 0) t0 = clock64();  // the end-phase bound counts idle time only
+    if (moved) t0 = clock64();  // the end-phase bound counts idle time only
   }
   if (timed_out && lane == 0) {
     // hand the producer a STOP so the consumers finish
@@ -254,7 +285,7 @@ __device__ void stream_producer(const SParams &P, StreamSmem &sm, unsigned char 
       const volatile StageMeta &d = sm.ring[it % kRing];
       mt.kind = d.kind; mt.b = d.b; mt.row = d.row; mt.tile = d.tile; mt.n = d.n;
       mt.isdraft = d.isdraft; mt.j = d.j; mt.c = d.c; mt.Mp = d.Mp; mt.invZp = d.invZp;
-      mt.Mq = d.Mq; mt.invZq = d.invZq;
+      mt.Mq = d.Mq; mt.invZq = d.invZq; mt.target = d.target;
       __threadfence_block();
       sm.ring_head = it + 1;
     }
@@ -322,24 +353,25 @@ __device__ void stream_producer(const SParams &P, StreamSmem &sm, unsigned char 
   }
 }
 
-// Bookkeeper: the tile partial merged from the kCW slice partials held by
-// lanes 0..kCW-1 (other lanes pass neutral values).  Returns it in lane 0.
-__device__ __forceinline__ float2 merge_slices(int kind, float2 v, float c) {
-  const bool mine = lane_id() < kCW;
-  if (kind == U_SOFTMAX) {
-    const float m = mine ? v.x : -CUDART_INF_F;
-    const float M = warp_max_nan(m);
-    float z = 0.f;
-    if (mine) z = (v.x == -CUDART_INF_F) ? v.y : v.y * ex2((v.x - M) * c);
-    return make_float2(M, warp_sum(z));
+// Bookkeeper: the tile partial of one unit from its kCW = 16 slice partials,
+// held by the 16 lanes of a half-warp (the two halves merge two units at
+// once).  Branch-free so both halves run the same shuffles whatever their
+// unit kinds: softmax (M, sum s 2^((m - M) c)), argmax (max, lowest index
+// holding it), residual (sum of masses, in .y).
+__device__ __forceinline__ float2 half_merge(int kind, float2 v, float c) {
+  float mx = v.x;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) mx = max_nan(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  float z = 0.f;
+  if (kind == U_SOFTMAX) z = (v.x == -CUDART_INF_F) ? v.y : v.y * ex2((v.x - mx) * c);
+  else if (kind == U_RESID) z = v.x;
+  int idx = (kind == U_ARGMAX && v.x == mx) ? __float_as_int(v.y) : 0x7fffffff;
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) {
+    z += __shfl_xor_sync(0xffffffffu, z, o);
+    idx = min(idx, __shfl_xor_sync(0xffffffffu, idx, o));
   }
-  if (kind == U_ARGMAX) {
-    const float m = mine ? v.x : -CUDART_INF_F;
-    const float best = warp_max_nan(m);
-    const int idx = warp_min_int(mine && v.x == best ? __float_as_int(v.y) : 0x7fffffff);
-    return make_float2(best, __int_as_float(idx));
-  }
-  return make_float2(warp_sum(mine ? v.x : 0.f), 0.f);
+  return make_float2(mx, kind == U_ARGMAX ? __int_as_float(idx) : z);
 }
 
 template <int MODE, int TDT, int DDT, bool PROBS>
@@ -353,8 +385,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1) sv_stream_kernel(const SPar
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.done[s], kCW);
-      mbar_init(&sm.empty[s], 1);
+      mbar_init(&sm.empty[s], kCW);
+    }
+    for (int s = 0; s < kPR; ++s) {
+      mbar_init(&sm.pdone[s], kCW);
+      mbar_init(&sm.pfree[s], 1);
     }
     sm.dq_push = 0;
     sm.dq_pop = 0;
@@ -379,6 +414,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) sv_stream_kernel(const SPar
 
   if (warp >= 4) {
     // ------------------------------------------------------------ consumers
+    // Each consumer warp releases the stage itself once its slice is reduced,
+    // then hands the slice partial to the bookkeeper through a ring of kPR
+    // partial slots (slot it % kPR for unit it).
     const int cw = warp - 4;
     for (int it = 0;; ++it) {
       const int s = it % kStages;
@@ -388,10 +426,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) sv_stream_kernel(const SPar
         return;
       }
       const StageMeta mt = sm.meta[s];
-      if (mt.kind == U_STOP) {
-        if (lane == 0) mbar_arrive(&sm.done[s]);
-        break;
-      }
       const unsigned char *st = stages + (size_t)s * kStageBytes;
       float2 part = make_float2(0.f, 0.f);
       if (mt.kind == U_SOFTMAX) {
@@ -402,88 +436,110 @@ __global__ void __launch_bounds__(kStreamThreads, 1) sv_stream_kernel(const SPar
       } else if (mt.kind == U_RESID) {
         if constexpr (MODE == MODE_CHAIN) part.x = warp_resid_slice<TDT, DDT, PROBS>(st, mt.n, cw, mt);
       }
+      __syncwarp();  // every lane is done with the stage
+      const int ps = it % kPR;
+      bool ok = true;
       if (lane == 0) {
-        sm.wpart[s][cw] = part;
-        mbar_arrive(&sm.done[s]);
+        if (mt.kind != U_STOP) mbar_arrive(&sm.empty[s]);
+        if (it >= kPR) ok = mbar_wait(&sm.pfree[ps], ((unsigned)(it / kPR) & 1u) ^ 1u, clock64());
+        if (ok) {
+          sm.wpart[ps][cw] = part;
+          if (cw == 0) sm.pmeta[ps] = mt;
+          mbar_arrive(&sm.pdone[ps]);
+        } else {
+          atomicOr(&P.hdr->error, 1u);
+        }
       }
-      __syncwarp();
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok || mt.kind == U_STOP) break;
     }
     return;
   }
 
   if (warp == 1) {
     // ------------------------------------------------------------ bookkeeper
+    // Drains the partial ring in batches of up to kBookBatch units: stores
+    // the slice partials and tile partials (two units per pass, one per
+    // half-warp), fences once, then adds each batch row's units to its
+    // counter with one atomic per row, issued by one leader lane per row.
+    const int half = lane >> 4, hl = lane & 15;
     bool stop = false;
     for (int it = 0; !stop;) {
-      const int s0 = it % kStages;
-      if (!mbar_wait(&sm.done[s0], (unsigned)(it / kStages) & 1u, clock64())) {
-        if (lane == 0) atomicOr(&P.hdr->error, 1u);
-        break;
-      }
       int nb = 1;
-      while (nb < kBookBatch &&
-             mbar_test(&sm.done[(it + nb) % kStages], (unsigned)((it + nb) / kStages) & 1u))
-        ++nb;
-      // Read the batch's descriptors and slice partials, release the stages,
-      // then write the partials out: the release never waits on global stores.
-      StageMeta mts[kBookBatch];
-      float2 wps[kBookBatch];
-      int used = 0;
-      for (int k = 0; k < nb; ++k) {
-        const int s = (it + k) % kStages;
-        mts[k] = sm.meta[s];
-        if (mts[k].kind == U_STOP) { stop = true; break; }
-        wps[k] = lane < kCW ? sm.wpart[s][lane] : make_float2(0.f, 0.f);
-        ++used;
-      }
-      __syncwarp();
-      if (lane == 0)
-        for (int k = 0; k < used; ++k) mbar_arrive(&sm.empty[(it + k) % kStages]);
-      __syncwarp();
-      unsigned *cnt[kBookBatch];
-      unsigned target[kBookBatch];
-      int item[kBookBatch];
-      for (int k = 0; k < used; ++k) {
-        const StageMeta &mt = mts[k];
-        const float2 wp = wps[k];
-        if (mt.kind == U_SOFTMAX || mt.kind == U_ARGMAX) {
-          const size_t ro = ((size_t)mt.b * P.rows + mt.row) * P.tilesMax + mt.tile;
-          if (lane < kCW) P.partA[ro * kCW + lane] = wp;
-          const float2 tp = merge_slices(mt.kind, wp, mt.c);
-          if (lane == 0) P.partT[ro] = tp;
-        } else if (mt.kind == U_RESID) {
-          const size_t ro = (size_t)mt.b * P.tilesB + mt.tile;
-          if (lane < kCW) P.partB[ro * kCW + lane] = wp.x;
-          const float2 tp = merge_slices(U_RESID, wp, 0.f);
-          if (lane == 0) P.partBT[ro] = tp.x;
-        }
-        if (mt.kind == U_SKIP) {
-          cnt[k] = nullptr;
-          target[k] = 0;
-          item[k] = 0;
-        } else if (mt.kind == U_RESID) {
-          cnt[k] = P.b_count + mt.b;
-          target[k] = (unsigned)P.tilesB;
-          item[k] = D_FINAL;
-        } else {
-          cnt[k] = P.a_count + mt.b;
-          target[k] = (unsigned)P.unitsA;
-          item[k] = (MODE == MODE_TREE) ? D_TREE : D_CHAIN;
-        }
-      }
-      __syncwarp();
       if (lane == 0) {
-        fence_acq_rel_gpu();  // the partials above before the arrivals below
-        unsigned prev[kBookBatch];
-        for (int k = 0; k < used; ++k) prev[k] = cnt[k] ? atomicAdd(cnt[k], 1u) : 0xffffffffu;
-        bool any_last = false;
-        for (int k = 0; k < used; ++k) any_last |= cnt[k] && (prev[k] == target[k] - 1);
-        if (any_last) fence_acq_rel_gpu();  // acquire: other CTAs' partials of the row
-        for (int k = 0; k < used; ++k) {
-          if (cnt[k] && prev[k] == target[k] - 1) {
+        if (!mbar_wait(&sm.pdone[it % kPR], (unsigned)(it / kPR) & 1u, clock64())) {
+          atomicOr(&P.hdr->error, 1u);
+          nb = 0;
+        }
+        while (nb > 0 && nb < kBookBatch &&
+               mbar_test(&sm.pdone[(it + nb) % kPR], (unsigned)((it + nb) / kPR) & 1u))
+          ++nb;
+      }
+      nb = __shfl_sync(0xffffffffu, nb, 0);
+      if (nb == 0) break;
+      // lane l < nb: unit it + l's row key, for the counting below
+      int kl = U_SKIP, bl = 0, tl = 0;
+      if (lane < nb) {
+        const StageMeta &m = sm.pmeta[(it + lane) % kPR];
+        kl = m.kind;
+        bl = m.b;
+        tl = (kl == U_RESID) ? P.tilesB : m.target;
+      }
+      const unsigned sm_stop = __ballot_sync(0xffffffffu, lane < nb && kl == U_STOP);
+      const int used = sm_stop ? __ffs(sm_stop) - 1 : nb;
+      stop = sm_stop != 0;
+      // partial stores and tile merges, two units per pass
+      for (int k0 = 0; k0 < used; k0 += 2) {
+        const int k = k0 + half;
+        int kind = U_SKIP, b = 0, ro = 0;
+        float c = 0.f;
+        float2 wp = make_float2(0.f, 0.f);
+        if (k < used) {
+          const StageMeta &m = sm.pmeta[(it + k) % kPR];
+          kind = m.kind;
+          b = m.b;
+          ro = (kind == U_RESID) ? m.tile : m.row * P.tilesMax + m.tile;
+          c = m.c;
+          wp = sm.wpart[(it + k) % kPR][hl];
+        }
+        const float2 tp = half_merge(kind, wp, c);
+        if (kind == U_SOFTMAX || kind == U_ARGMAX) {
+          const size_t r = (size_t)b * P.rows * P.tilesMax + ro;
+          P.partA[r * kCW + hl] = wp;
+          if (hl == 0) P.partT[r] = tp;
+        } else if (kind == U_RESID) {
+          const size_t r = (size_t)b * P.tilesB + ro;
+          P.partB[r * kCW + hl] = wp.x;
+          if (hl == 0) P.partBT[r] = tp.y;
+        }
+      }
+      __syncwarp();
+      fence_acq_rel_gpu();  // the partials above before the counts below
+      // one leader lane per (counter, row) adds that row's units of the batch
+      const bool counted = lane < used && kl != U_SKIP;
+      const unsigned key = counted ? ((kl == U_RESID ? 0x80000000u : 0u) | (unsigned)bl)
+                                   : (0x40000000u | (unsigned)lane);
+      const unsigned grp = __match_any_sync(0xffffffffu, key);
+      bool last = false;
+      if (counted && (__ffs(grp) - 1) == lane) {
+        const unsigned n = (unsigned)__popc(grp);
+        const unsigned prev = atomicAdd((kl == U_RESID ? P.b_count : P.a_count) + bl, n);
+        last = prev + n == (unsigned)tl;
+      }
+      const unsigned lm = __ballot_sync(0xffffffffu, last);
+      if (lane == 0)
+        for (int k = 0; k < used; ++k) mbar_arrive(&sm.pfree[(it + k) % kPR]);
+      if (lm) {
+        fence_acq_rel_gpu();  // acquire: other CTAs' partials of the completed rows
+        for (unsigned mm = lm; mm; mm &= mm - 1) {
+          const int l = __ffs(mm) - 1;
+          const int kind = __shfl_sync(0xffffffffu, kl, l);
+          const int b = __shfl_sync(0xffffffffu, bl, l);
+          if (lane == 0) {
+            const int item = kind == U_RESID ? D_FINAL : (MODE == MODE_TREE ? D_TREE : D_CHAIN);
             const long long tq = clock64();
             while (sm.dq_push - sm.dq_pop >= kDQ && clock64() - tq < kStreamWait) __nanosleep(64);
-            reinterpret_cast<volatile int *>(sm.dq)[sm.dq_push % kDQ] = (item[k] << 28) | mts[k].b;
+            reinterpret_cast<volatile int *>(sm.dq)[sm.dq_push % kDQ] = (item << 28) | b;
             __threadfence_block();
             sm.dq_push = sm.dq_push + 1;
           }

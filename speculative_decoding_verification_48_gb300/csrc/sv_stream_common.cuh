@@ -13,7 +13,8 @@ constexpr int kStreamThreads = kStreamWarps * 32;  // 640
 constexpr int kStages = 6;
 constexpr int kStageBytes = 32768;
 constexpr int kDQ = 64;                            // decider queue entries
-constexpr int kBookBatch = 4;                      // stages per bookkeeper fence
+constexpr int kBookBatch = 16;                     // units per bookkeeper fence (<= 32)
+constexpr int kPR = 32;                            // slice-partial ring (consumers -> bookkeeper)
 constexpr int kClaim = 8;                          // Phase-A units per claim
 constexpr int kPoll = 8;                           // units between queue-counter polls
 constexpr int kRing = 16;                          // scheduler -> producer descriptors
@@ -70,15 +71,19 @@ struct SParams {
   float *partBT;   // [B][tilesB]               residual mass per tile
 };
 
+// Unit descriptor.  `target` is the number of Phase-A units that complete
+// the unit's batch row (units the scheduler does not emit are not counted).
 struct StageMeta {
-  int kind, b, row, tile, n, isdraft, j, pad;
+  int kind, b, row, tile, n, isdraft, j, target;
   float c, Mp, invZp, Mq, invZq, pad2[3];
 };
 
 struct alignas(16) StreamSmem {
-  uint64_t full[kStages], done[kStages], empty[kStages];
+  uint64_t full[kStages], empty[kStages];  // producer <-> consumers, per stage
+  uint64_t pdone[kPR], pfree[kPR];         // consumers <-> bookkeeper, per partial slot
   StageMeta meta[kStages];
-  float2 wpart[kStages][kCW];
+  StageMeta pmeta[kPR];
+  float2 wpart[kPR][kCW];
   int dq[kDQ];
   volatile int dq_push, dq_pop, ctl_done, pad;
   StageMeta ring[kRing];
@@ -207,6 +212,10 @@ __device__ __forceinline__ void slice_load(const unsigned char *stage, int cw, i
   }
 }
 
+// (m, s): m = slice max, s = sum exp2((v - m) c).  The exponent argument is
+// one FFMA, v c - mc with mc = round(m c); that shifts every term of the
+// slice by the same factor 2^d, d = m c - mc (computed exactly with an FMA),
+// which is divided out once.  Overflowing m c falls back to (v - m) c.
 template <int DT>
 __device__ __forceinline__ float2 warp_softmax_slice(const unsigned char *stage, int n, int cw,
                                                      float c) {
@@ -216,13 +225,22 @@ __device__ __forceinline__ float2 warp_softmax_slice(const unsigned char *stage,
   float m4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
 #pragma unroll
   for (int i = 0; i < PER; ++i) m4[i & 3] = max_nan(m4[i & 3], v[i]);
-  float m = warp_max_nan(max_nan(max_nan(m4[0], m4[1]), max_nan(m4[2], m4[3])));
+  const float m = warp_max_nan(max_nan(max_nan(m4[0], m4[1]), max_nan(m4[2], m4[3])));
   float s4[4] = {0.f, 0.f, 0.f, 0.f};
+  float scale = 1.f;
   if (m != -CUDART_INF_F) {
+    const float mc = m * c;
+    if (fabsf(mc) <= 1.0e37f) {
+      const float d = fmaf(m, c, -mc);
 #pragma unroll
-    for (int i = 0; i < PER; ++i) s4[i & 3] += ex2((v[i] - m) * c);
+      for (int i = 0; i < PER; ++i) s4[i & 3] += ex2(fmaf(v[i], c, -mc));
+      scale = ex2(-d);
+    } else {
+#pragma unroll
+      for (int i = 0; i < PER; ++i) s4[i & 3] += ex2((v[i] - m) * c);
+    }
   }
-  return make_float2(m, warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3])));
+  return make_float2(m, warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3])) * scale);
 }
 
 template <int DT>
