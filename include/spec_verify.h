@@ -177,6 +177,45 @@ SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
 /* Static description of a status code; never NULL. */
 SV_API const char *spec_verify_status_string(sv_status s);
 
+/*
+ * Bytes of the fixed scratch array behind spec_verify_chain_no_alloc.
+ */
+#define SV_NO_ALLOC_SCRATCH_BYTES (8 << 20)
+
+/*
+ * spec_verify_chain without a caller-provided workspace.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory — for example a plugin inside a serving engine that has
+ * already reserved the whole GPU for its own pool, or a decode loop that must
+ * not call cudaMalloc because cudaMalloc can synchronise the device.  Inputs
+ * and outputs are the caller's device arrays, exactly as for
+ * spec_verify_chain (same arguments, same results); only the scratch memory
+ * differs.  It is one fixed array of SV_NO_ALLOC_SCRATCH_BYTES (8 MiB) in the
+ * library's device image, which every GPU that loads the library holds until
+ * the process exits.  This function allocates nothing and calls no
+ * allocating library routine.
+ *
+ *  - Sizes whose workspace (spec_verify_workspace_bytes with rows_per_batch
+ *    2*gamma+1, or gamma+1 with draft_is_probs) exceeds
+ *    SV_NO_ALLOC_SCRATCH_BYTES return SV_ERR_UNSUPPORTED and enqueue nothing.
+ *    B=64, gamma=7, V=128256 needs about 2 MB.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.  A failed lookup returns SV_ERR_CUDA.
+ *  - Every call on a device shares the one array.  Calls that may overlap
+ *    on the GPU (different streams, or different host threads without
+ *    ordering) race on it and give wrong results: keep them in one stream
+ *    order.  Each call zeroes the array's control block before its kernel
+ *    runs, so what an earlier call left there does no harm.
+ */
+SV_API sv_status spec_verify_chain_no_alloc(const void *target_logits, sv_dtype tdt,
+                                            const void *draft, sv_dtype ddt, int draft_is_probs,
+                                            const int32_t *draft_tokens,
+                                            const float *temperatures, const float *uniforms,
+                                            int B, int gamma, int V, int32_t *out_tokens,
+                                            int32_t *out_num_accepted, float *out_diag,
+                                            int32_t *out_row_status, sv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
