@@ -4,7 +4,7 @@
 #include <atomic>
 #include <cstdlib>
 
-#include "sv_stream.cuh"
+#include "sv_pass_common.cuh"
 
 namespace sv {
 
@@ -21,8 +21,8 @@ int sm_count(int device) {
 
 size_t workspace_bytes_any(int B, int rows, int V) {
   const size_t a = make_layout(B, rows, V).total;
-  // smallest tiles (fp32 rows) give the most partials
-  const size_t b = make_stream_layout(B, rows, V, 4, 4, false).total;
+  // fp32 rows give the most warp-chunks
+  const size_t b = make_pass_layout(B, rows, V, 4, 4, true).total;
   return a > b ? a : b;
 }
 

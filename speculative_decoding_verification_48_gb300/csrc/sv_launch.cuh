@@ -1,9 +1,10 @@
-// Host-side launch of the persistent verification kernel.
+// Host-side launches: the two-launch path for 16-byte-aligned rows, the
+// register-tile kernels (two phases) for any other shape.
 #pragma once
 
 #include <atomic>
 
-#include "sv_stream.cuh"
+#include "sv_pass_decide.cuh"
 
 namespace sv {
 
@@ -36,25 +37,43 @@ sv_status launch_phase(const KParams &P0, const Sched &s, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-// Streaming kernel: one persistent CTA per SM.
+// Stats units (warp-chunks) of the two-launch path for this call; -1 if the
+// count does not fit the kernels' 32-bit unit indices.
 template <int MODE, int TDT, int DDT, bool PROBS>
-sv_status launch_stream(const KParams &P0, cudaStream_t stream) {
-  auto kern = sv_stream_kernel<MODE, TDT, DDT, PROBS>;
-  static std::atomic<int> attr_done[kMaxDevices];
+long long pass_units(const KParams &P, const PassLayout &L) {
+  long long total;
+  if (MODE == MODE_TREE) total = (long long)P.B * P.N * L.cT;
+  else total = (long long)P.B * L.cT + (long long)P.gamma * P.B * (L.cT + L.cD);
+  return total < (1LL << 31) - 1 ? total : -1;
+}
+
+// Two-launch path: the stats kernel over every needed row, then the decide
+// kernel as its programmatic dependent (its CTAs launch while the stats
+// kernel drains and wait on the device for its completion).
+template <int MODE, int TDT, int DDT, bool PROBS>
+sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
+                      cudaStream_t stream) {
+  auto stats = sv_stats_kernel<MODE, TDT, DDT, PROBS>;
+  auto decide = sv_decide_kernel<MODE, TDT, DDT, PROBS>;
+  static std::atomic<int> occ_cache[kMaxDevices], occd_cache[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
-  if (!attr_done[dev].load(std::memory_order_relaxed)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kStreamSmemBytes) != cudaSuccess)
+  int occ = occ_cache[dev].load(std::memory_order_relaxed);
+  int occd = occd_cache[dev].load(std::memory_order_relaxed);
+  if (occ == 0 || occd == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, stats, kPassThreads, 0) != cudaSuccess ||
+        occ <= 0 ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occd, decide, kPassThreads, 0) !=
+            cudaSuccess ||
+        occd <= 0)
       return SV_ERR_CUDA;
-    attr_done[dev].store(1, std::memory_order_relaxed);
+    occ_cache[dev].store(occ, std::memory_order_relaxed);
+    occd_cache[dev].store(occd, std::memory_order_relaxed);
   }
   const int sms = sm_count(dev);
   if (sms <= 0) return SV_ERR_CUDA;
-  const int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
-  const StreamLayout L = make_stream_layout(P0.B, P0.rows, P0.V, esT, esD, PROBS);
   char *w = reinterpret_cast<char *>(P0.hdr);
-  SParams S{};
+  PassParams S{};
   S.target = P0.target;
   S.draft = P0.draft;
   S.draft_tokens = P0.draft_tokens;
@@ -68,38 +87,55 @@ sv_status launch_stream(const KParams &P0, cudaStream_t stream) {
   S.N = P0.N;
   S.max_depth = P0.max_depth;
   S.rows = P0.rows;
-  S.tilesT = L.tilesT;
-  S.tilesD = L.tilesD;
-  S.tilesMax = L.tilesMax;
-  S.tilesB = L.tilesB;
-  S.TA_T = L.TA_T;
-  S.TA_D = L.TA_D;
-  S.TB = L.TB;
+  S.cT = L.cT;
+  S.cD = L.cD;
+  S.cMax = L.cMax;
+  S.cR = L.cR;
+  int H = 1;
   if (MODE == MODE_CHAIN) {
-    const int G1 = P0.gamma + 1;
-    S.unitsA = G1 * L.tilesT + (PROBS ? 0 : P0.gamma * L.tilesD);
-  } else {
-    S.unitsA = P0.rows * L.tilesT;
+    // about 16 residual chunks per decide CTA (one step of two chunks per
+    // warp), while the decide grid stays within one wave of resident CTAs
+    H = (L.cR + 15) / 16;
+    const int cap = (occd * sms) / P0.B;
+    if (H > cap) H = cap;
+    if (H > 32) H = 32;
+    if (H < 1) H = 1;
   }
-  S.totalA = P0.B * S.unitsA;
+  S.H = H;
+  S.total = (int)total;
+  S.fd_cT = make_fastdiv((unsigned)L.cT);
+  S.fd_cP = make_fastdiv((unsigned)(L.cT + L.cD));
+  S.fd_blk = make_fastdiv((unsigned)((long long)P0.B * (L.cT + L.cD) < (1LL << 31)
+                                         ? P0.B * (L.cT + L.cD) : 1));
+  S.fd_N = make_fastdiv((unsigned)(P0.N > 0 ? P0.N : 1));
   S.out_tokens = P0.out_tokens;
   S.out_nacc = P0.out_nacc;
   S.out_status = P0.out_status;
   S.out_path = P0.out_path;
   S.out_diag = P0.out_diag;
-  S.hdr = reinterpret_cast<StreamHeader *>(w);
-  S.a_count = reinterpret_cast<unsigned *>(w + L.a_count);
-  S.b_count = reinterpret_cast<unsigned *>(w + L.b_count);
-  S.row_done = reinterpret_cast<unsigned *>(w + L.row_done);
-  S.qitems = reinterpret_cast<unsigned *>(w + L.qitems);
-  S.dec = reinterpret_cast<Decision *>(w + L.dec);
-  S.partA = reinterpret_cast<float2 *>(w + L.partA);
-  S.partB = reinterpret_cast<float *>(w + L.partB);
-  S.partT = reinterpret_cast<float2 *>(w + L.partT);
-  S.partBT = reinterpret_cast<float *>(w + L.partBT);
+  S.claim = reinterpret_cast<unsigned *>(w + L.claim);
+  S.done = reinterpret_cast<unsigned *>(w + L.done);
+  S.part = reinterpret_cast<float2 *>(w + L.part);
+  S.resid = reinterpret_cast<float *>(w + L.resid);
+  const long long want = (total + kPassWarps - 1) / kPassWarps;
+  const long long cap = (long long)sms * occ;
+  int grid = (int)(want < cap ? want : cap);
+  if (grid < 1) grid = 1;
   if (cudaMemsetAsync(w, 0, L.ctrl, stream) != cudaSuccess) return SV_ERR_CUDA;
-  kern<<<sms, kStreamThreads, kStreamSmemBytes, stream>>>(S);
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  stats<<<grid, kPassThreads, 0, stream>>>(S);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(P0.B * H));
+  cfg.blockDim = dim3(kPassThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decide, S) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
 }
 
 // Rows of both logit arrays start on 16-byte boundaries.
@@ -110,12 +146,16 @@ inline bool rows_aligned(const void *p, int V, int es) {
 template <int MODE, int TDT, int DDT, bool PROBS>
 sv_status launch_verify(const KParams &P, cudaStream_t stream) {
   {
-    const int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
+    constexpr int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
     bool ok = rows_aligned(P.target, P.V, esT);
     if (MODE == MODE_CHAIN) ok = ok && rows_aligned(P.draft, P.V, esD);
-    // Phase-B queue items pack b * tilesB + t in 27 bits
-    if (MODE == MODE_CHAIN) ok = ok && (long long)P.B * ((P.V + 4095) / 4096) < (1LL << 26);
-    if (ok && P.use_stream) return launch_stream<MODE, TDT, DDT, PROBS>(P, stream);
+    if (ok && P.use_stream) {
+      const PassLayout L =
+          make_pass_layout(P.B, P.rows, P.V, esT, esD, MODE == MODE_CHAIN && !PROBS);
+      const long long total = pass_units<MODE, TDT, DDT, PROBS>(P, L);
+      if (total >= 0 && (long long)P.B * 16 < (1LL << 31))
+        return launch_pass<MODE, TDT, DDT, PROBS>(P, L, total, stream);
+    }
   }
   const int B = P.B, A = P.rows * P.tiles;
   if (cudaMemsetAsync(P.hdr, 0, P.ctrl_bytes, stream) != cudaSuccess) return SV_ERR_CUDA;

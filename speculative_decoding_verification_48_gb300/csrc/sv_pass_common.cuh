@@ -1,0 +1,273 @@
+// Shared definitions of the two-launch verification path for rows that start
+// on 16-byte boundaries: chunk geometry, parameters, workspace layout, vector
+// loads and warp-level merge / crossing helpers.
+//
+//   sv_stats_kernel   streams every logit row once.  Each warp reduces
+//                     "warp-chunks" of 2 KB (32 lanes x 4 x 16-byte vectors)
+//                     to a partial — (max, sum exp2) for a softmax row,
+//                     (max, first index) for an argmax row — and stores it.
+//                     Warps are independent: no block barrier, no atomics.
+//   sv_decide_kernel  launched as a programmatic dependent of the first:
+//                     merges the partials of each batch row, runs the accept
+//                     tests / greedy match / tree walk, draws the bonus token
+//                     from the partials of row gamma, and splits the residual
+//                     sweep of a rejected row pair over several CTAs; the
+//                     last of them finds the crossing chunk and rescans it.
+#pragma once
+
+#include "sv_kernel.cuh"
+
+namespace sv {
+
+constexpr int kPassThreads = 256;
+constexpr int kPassWarps = kPassThreads / 32;
+constexpr int kChunkBytes = 2048;  // one warp-chunk
+constexpr int kChunkVecs = 4;      // 16-byte vectors per lane per warp-chunk
+constexpr int kClaimStripes = 16;  // stats-kernel claim counters
+constexpr int kClaimStride = 32;   // 128 bytes between counters
+constexpr int kClaimProbes = 4096; // bound of the end-of-work probe loop
+
+template <int DT> struct Chunk {
+  static constexpr int kEs = (int)sizeof(typename Elt<DT>::T);
+  static constexpr int kVec = 16 / kEs;             // elements per 16-byte vector
+  static constexpr int kElems = kChunkBytes / kEs;  // 1024 (2-byte types) or 512
+  static constexpr int kPer = kElems / 32;          // elements per lane
+};
+
+// Residual chunks of a row pair: 2 KB of the wider of the two element types.
+template <int TDT, int DDT> struct PairChunk {
+  static constexpr int kEs = Chunk<TDT>::kEs > Chunk<DDT>::kEs ? Chunk<TDT>::kEs : Chunk<DDT>::kEs;
+  static constexpr int kElems = kChunkBytes / kEs;
+  static constexpr int kVec = 16 / kEs;   // elements per vector, both rows
+  static constexpr int kVecs = kElems / (32 * kVec);
+  static constexpr int kPer = kElems / 32;
+};
+
+// Quotient by a divisor that is fixed for a call, without a hardware divide
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, floor(n / d) = (umulhi(n, m) + n) >> l,
+// exact for 0 <= n < 2^31 and 1 <= d < 2^31 (the sum then fits 32 bits).
+struct FastDiv {
+  unsigned d, m, l;
+};
+
+inline FastDiv make_fastdiv(unsigned d) {
+  unsigned l = 0;
+  while ((1ull << l) < d) ++l;
+  const unsigned long long m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+  return FastDiv{d, (unsigned)m, l};
+}
+
+__device__ __forceinline__ unsigned fdiv(unsigned n, const FastDiv &f) {
+  return (__umulhi(n, f.m) + n) >> f.l;
+}
+
+struct PassParams {
+  const void *target;  // chain: [B, gamma+1, V]; tree: [B*N, V]
+  const void *draft;   // [B, gamma, V] logits or fp32 probabilities
+  const int32_t *draft_tokens;
+  const float *temps;
+  const float *unif;
+  const int32_t *parent;
+  const int32_t *node_tokens;
+  int B, gamma, V, N, max_depth, rows;
+  int cT, cD, cMax;  // warp-chunks per target row / draft row (0 if not streamed) / max
+  int cR;            // residual chunks per row pair
+  int H;             // decide CTAs per batch row
+  int total;         // stats units (warp-chunks, skipped ones included)
+  FastDiv fd_cT, fd_cP, fd_blk, fd_N;  // divisors of the unit decode: cT, cT + cD, B (cT + cD), N
+  int32_t *out_tokens, *out_nacc, *out_status, *out_path;
+  float *out_diag;
+  unsigned *claim;   // [kClaimStripes * kClaimStride] stats-kernel claim counters, then an
+                     // error word (nonzero: the claim probe bound was hit)
+  unsigned *done;    // [B] residual-sweep arrivals
+  float2 *part;      // [B][rows][cMax] warp-chunk partials
+  float *resid;      // [B][cR] residual mass per chunk of the rejected row pair
+};
+
+// Workspace: claim counters, done[B] (together the control block [0, ctrl),
+// zeroed by every call), partials, residual chunk sums.
+struct PassLayout {
+  size_t claim, done, ctrl, part, resid, total;
+  int cT, cD, cMax, cR;
+};
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+inline PassLayout make_pass_layout(int B, int rows, int V, int esT, int esD, bool stream_draft) {
+  PassLayout L;
+  L.cT = ceil_div(V, kChunkBytes / esT);
+  L.cD = stream_draft ? ceil_div(V, kChunkBytes / esD) : 0;
+  L.cMax = L.cT > L.cD ? L.cT : L.cD;
+  L.cR = ceil_div(V, kChunkBytes / (esT > esD ? esT : esD));
+  size_t off = 0;
+  L.claim = off; off += (size_t)(kClaimStripes + 1) * kClaimStride * 4;
+  L.done = off;  off = align_up(off + (size_t)B * 4, 256);
+  L.ctrl = off;
+  L.part = off;  off = align_up(off + (size_t)B * rows * L.cMax * sizeof(float2), 256);
+  L.resid = off; off = align_up(off + (size_t)B * L.cR * sizeof(float), 256);
+  L.total = off;
+  return L;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p) {
+  return *reinterpret_cast<const volatile unsigned *>(p);
+}
+
+// 16-byte streaming load through the non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_nc16(const void *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ld_nc8(const void *p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(r.x), "=r"(r.y)
+               : "l"(p));
+  return r;
+}
+
+// VEC elements of dtype DT starting at p (VEC * size = 8 or 16 bytes, aligned).
+template <int DT, int VEC>
+__device__ __forceinline__ void vec_load(const typename Elt<DT>::T *p, float *o) {
+  constexpr int kB = VEC * (int)sizeof(typename Elt<DT>::T);
+  static_assert(kB == 16 || kB == 8, "vector loads are 8 or 16 bytes");
+  if constexpr (kB == 16) Elt<DT>::unpack(ld_nc16(p), o);
+  else Elt<DT>::unpack(ld_nc8(p), o);
+}
+
+// One raw vector of VEC elements of DT (8 or 16 bytes), loaded now and
+// unpacked when used.
+template <int DT, int VEC> struct RawVec {
+  static constexpr int kB = VEC * (int)sizeof(typename Elt<DT>::T);
+  static_assert(kB == 16 || kB == 8, "vector loads are 8 or 16 bytes");
+  using R = typename std::conditional<kB == 16, uint4, uint2>::type;
+  R r;
+  __device__ __forceinline__ void load(const typename Elt<DT>::T *p) {
+    if constexpr (kB == 16) r = ld_nc16(p);
+    else r = ld_nc8(p);
+  }
+  __device__ __forceinline__ void unpack(float *o) const { Elt<DT>::unpack(r, o); }
+};
+
+// Residual term max(0, p(x) - q(x)) of the sweep, with each side's
+// normaliser folded into its exponent: p(x) = 2^(l_p(x) c + a_p),
+// a_p = -(M_p c + log2 Z_p), one FFMA and one ex2 per side (q is read as
+// given for probability drafts).  Identical rows give identical p and q,
+// hence exactly zero; NaN propagates.
+struct ResidCoef {
+  float c, ap, aq;
+};
+template <bool PROBS>
+__device__ __forceinline__ float resid_term(float lp, float lq, const ResidCoef &k) {
+  const float p = ex2(fmaf(lp, k.c, k.ap));
+  const float q = PROBS ? lq : ex2(fmaf(lq, k.c, k.aq));
+  return max_nan(0.f, p - q);
+}
+
+// Wait for the grid this one depends on (programmatic dependent launch);
+// returns at once when the launch had no such dependency.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the dependent grid start launching (its CTAs still wait in
+// grid_dependency_wait until this grid has completed and flushed).
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Softmax merge of two partials (m, s), s = sum 2^((x - m) c).  -inf maxima
+// carry no mass; NaN anywhere gives NaN.
+__device__ __forceinline__ float2 softmax_merge(float2 a, float2 b, float c) {
+  const float M = max_nan(a.x, b.x);
+  const float za = (a.x == -CUDART_INF_F) ? 0.f : a.y * ex2((a.x - M) * c);
+  const float zb = (b.x == -CUDART_INF_F) ? 0.f : b.y * ex2((b.x - M) * c);
+  return make_float2(M, za + zb);
+}
+
+// Merge of one softmax row's `cnt` chunk partials by the whole warp: lanes
+// take chunks lane, lane + 32, ... (eight loads in flight per lane), then the
+// lane results are combined.  Returns (M, Z) with Z = sum_x 2^((x - M) c).
+__device__ __forceinline__ float2 warp_row_softmax(const float2 *part, int cnt, float c) {
+  const int lane = lane_id();
+  float2 acc = make_float2(-CUDART_INF_F, 0.f);
+  for (int i0 = 0; i0 < cnt; i0 += 256) {
+    float2 pt[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = i0 + lane + 32 * k;
+      pt[k] = i < cnt ? __ldcg(part + i) : make_float2(-CUDART_INF_F, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc = softmax_merge(acc, pt[k], c);
+  }
+  const float M = warp_max_nan(acc.x);
+  const float z = (acc.x == -CUDART_INF_F) ? 0.f : acc.y * ex2((acc.x - M) * c);
+  return make_float2(M, warp_sum(z));
+}
+
+// Two softmax rows merged by one warp with the loads of both in flight at
+// once (each row at most 256 chunks); `pb2` may be null.
+__device__ __forceinline__ void warp_rows_softmax2(const float2 *pa, int ca, const float2 *pb2,
+                                                   int cb, float c, float2 &ra, float2 &rb) {
+  const int lane = lane_id();
+  float2 xa[8], xb[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int i = lane + 32 * k;
+    xa[k] = i < ca ? __ldcg(pa + i) : make_float2(-CUDART_INF_F, 0.f);
+    xb[k] = (pb2 && i < cb) ? __ldcg(pb2 + i) : make_float2(-CUDART_INF_F, 0.f);
+  }
+  float2 aa = make_float2(-CUDART_INF_F, 0.f), ab = aa;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    aa = softmax_merge(aa, xa[k], c);
+    ab = softmax_merge(ab, xb[k], c);
+  }
+  const float Ma = warp_max_nan(aa.x), Mb = warp_max_nan(ab.x);
+  const float za = (aa.x == -CUDART_INF_F) ? 0.f : aa.y * ex2((aa.x - Ma) * c);
+  const float zb = (ab.x == -CUDART_INF_F) ? 0.f : ab.y * ex2((ab.x - Mb) * c);
+  ra = make_float2(Ma, warp_sum(za));
+  rb = make_float2(Mb, warp_sum(zb));
+}
+
+// Merge of one argmax row's chunk partials (value, global first index): the
+// largest value, and the lowest index among chunks holding it.  NaN anywhere
+// gives a NaN value.
+__device__ __forceinline__ float2 warp_row_argmax(const float2 *part, int cnt) {
+  const int lane = lane_id();
+  float best = -CUDART_INF_F;
+  int idx = 0x7fffffff;
+  bool nan = false;
+  for (int i0 = 0; i0 < cnt; i0 += 256) {
+    float2 pt[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = i0 + lane + 32 * k;
+      pt[k] = i < cnt ? __ldcg(part + i) : make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      nan |= isnan(pt[k].x);
+      const int ik = __float_as_int(pt[k].y);
+      if (pt[k].x > best || (pt[k].x == best && ik < idx)) {
+        best = pt[k].x;
+        idx = ik;
+      }
+    }
+  }
+  const bool anynan = __any_sync(0xffffffffu, nan);
+  const float M = warp_max_nan(best);
+  const int I = warp_min_int(best == M ? idx : 0x7fffffff);
+  return make_float2(anynan ? CUDART_NAN_F : M, __int_as_float(I));
+}
+
+}  // namespace sv

@@ -1,0 +1,355 @@
+// Decision pass: one group of H CTAs per batch row (one CTA per tree).
+//
+// Chain rows ("論文解説: Speculative Sampling", §技術的詳細 ステップ3: accept
+// draft i iff u_i q_i(x_i) < p_i(x_i), in order, stop at the first
+// rejection; §修正付き棄却サンプリング: the replacement is drawn from
+// norm(max(0, p_j - q_j)); §期待される高速化: gamma + 1 tokens per round, so a
+// row whose drafts all pass draws a bonus token from p_gamma).  Greedy rows
+// ("投機的デコーディングとは？" §ドラフト生成と並列検証の仕組み) accept while the
+// draft is the target's top token and emit the top token at the first
+// mismatch.  Trees (SpecInfer explainer, §技術の仕組み › 基本アイデア and
+// §推論方法) walk from the root along the child whose token is the current
+// node's top token.
+#pragma once
+
+#include "sv_pass_stats.cuh"
+
+namespace sv {
+
+struct DecideSmem {
+  float rowM[kMaxRows], rowZ[kMaxRows];
+  int rowI[kMaxRows];
+  int j, status, last;
+};
+
+struct TreeSmem {
+  int a[SV_MAX_TREE_NODES], par[SV_MAX_TREE_NODES], tok[SV_MAX_TREE_NODES];
+  int path[32];
+  int flags;
+};
+
+// Writes an invalid row: every token (and path entry) -1, no draft accepted.
+__device__ __forceinline__ void pass_error_row(const PassParams &P, int b, int status, int width,
+                                               int32_t *tok, int32_t *path) {
+  for (int s = lane_id(); s < width; s += 32) {
+    tok[s] = -1;
+    if (path) path[s] = -1;
+  }
+  if (lane_id() == 0) {
+    P.out_nacc[b] = 0;
+    if (P.out_status) P.out_status[b] = status;
+  }
+}
+
+// Chain rows.  Every CTA of the row merges the partials it needs and makes
+// the decision (cheap, from L2); CTA h = 0 writes the diagnostics and, for
+// greedy, bonus and invalid rows, the outputs.  A rejected row's residual
+// sweep is split over the H CTAs; the last to finish draws the token.  Every
+// step issues all of its loads at once, so the row costs a handful of
+// dependent round trips: gathers (before the wait on the stats kernel),
+// partials, sweep, arrival, residual sums, rescan.
+template <int MODE, int TDT, int DDT, bool PROBS>
+__device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &sm) {
+  using TT = typename Elt<TDT>::T;
+  using DTy = typename Elt<DDT>::T;
+  const int g = P.gamma, G1 = g + 1, V = P.V;
+  const int lane = lane_id(), warp = warp_id();
+  int32_t *ot = P.out_tokens + (size_t)b * G1;
+  const TT *tgt = reinterpret_cast<const TT *>(P.target) + (size_t)b * G1 * V;
+  // 0. inputs only (none is written by the stats kernel): issued before the
+  // wait so their latency overlaps the stats kernel's tail
+  const float T = (MODE == MODE_CHAIN) ? __ldg(P.temps + b) : 0.f;
+  const bool badT = bad_temperature(T);
+  const bool greedy = T <= 0.f;
+  const float c = kLog2e / T;
+  if ((badT || greedy) && h != 0) return;  // nothing to sweep
+  const int i = lane;
+  const bool act = warp == 0 && i < g;
+  int x = 0;
+  bool tok_ok = false;
+  float lp = 0.f, lq = 0.f, qp = 0.f, ui = 0.f;
+  if (act) {
+    x = __ldg(P.draft_tokens + (size_t)b * g + i);
+    tok_ok = x >= 0 && x < V;
+    if (!badT && !greedy && tok_ok) {
+      lp = Elt<TDT>::load1(tgt + (size_t)i * V + x);
+      if (PROBS) qp = __ldg(reinterpret_cast<const float *>(P.draft) + ((size_t)b * g + i) * V + x);
+      else lq = Elt<DDT>::load1(reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + i) * V + x);
+      ui = __ldg(P.unif + (size_t)b * G1 + i);
+    }
+  }
+  grid_dependency_wait();
+  if (badT) {
+    if (warp == 0) {
+      pass_error_row(P, b, SV_ROW_BAD_TEMPERATURE, G1, ot, nullptr);
+      if (MODE == MODE_CHAIN && P.out_diag)
+        for (int k = lane; k < g; k += 32)
+          reinterpret_cast<float4 *>(P.out_diag)[(size_t)b * g + k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  // 1. row merges: each warp takes rows warp, warp + 8, ... two at a time
+  const int nrows = greedy ? G1 : (PROBS ? G1 : 2 * g + 1);
+  const float2 *pb = P.part + (size_t)b * P.rows * P.cMax;
+  for (int r = warp; r < nrows; r += 2 * kPassWarps) {
+    const int r2 = r + kPassWarps;
+    const int ca = r < G1 ? P.cT : P.cD, cb = r2 < G1 ? P.cT : P.cD;
+    if (greedy) {
+      const float2 ma = warp_row_argmax(pb + (size_t)r * P.cMax, ca);
+      float2 mb = make_float2(0.f, 0.f);
+      if (r2 < nrows) mb = warp_row_argmax(pb + (size_t)r2 * P.cMax, cb);
+      if (lane == 0) {
+        sm.rowM[r] = ma.x; sm.rowI[r] = __float_as_int(ma.y);
+        if (r2 < nrows) { sm.rowM[r2] = mb.x; sm.rowI[r2] = __float_as_int(mb.y); }
+      }
+    } else {
+      float2 za, zb = make_float2(0.f, 0.f);
+      if (ca <= 256 && cb <= 256) {
+        warp_rows_softmax2(pb + (size_t)r * P.cMax, ca,
+                           r2 < nrows ? pb + (size_t)r2 * P.cMax : nullptr, cb, c, za, zb);
+      } else {
+        za = warp_row_softmax(pb + (size_t)r * P.cMax, ca, c);
+        if (r2 < nrows) zb = warp_row_softmax(pb + (size_t)r2 * P.cMax, cb, c);
+      }
+      if (lane == 0) {
+        sm.rowM[r] = za.x; sm.rowZ[r] = za.y;
+        if (r2 < nrows) { sm.rowM[r2] = zb.x; sm.rowZ[r2] = zb.y; }
+      }
+    }
+  }
+  __syncthreads();
+  // 2. accept tests (one lane per draft) and the first-reject scan
+  if (warp == 0) {
+    const unsigned gmask = (g >= 32) ? 0xffffffffu : ((1u << g) - 1u);
+    int status, j;
+    bool nf = false;
+    if (greedy) {
+      for (int r = lane; r < G1; r += 32) nf |= isnan(sm.rowM[r]);
+      const bool match = act && tok_ok && x == sm.rowI[i];
+      const unsigned mm = __ballot_sync(0xffffffffu, match) & gmask;
+      const unsigned badtok = __ballot_sync(0xffffffffu, act && !tok_ok);
+      const unsigned nfm = __ballot_sync(0xffffffffu, nf);
+      j = (~mm & gmask) ? __ffs(~mm & gmask) - 1 : g;
+      status = (badtok ? SV_ROW_BAD_TOKEN : 0) | (nfm ? SV_ROW_NONFINITE : 0);
+      if (MODE == MODE_CHAIN && act && P.out_diag)
+        reinterpret_cast<float4 *>(P.out_diag)[(size_t)b * g + i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      float p = 0.f, q = 0.f;
+      bool acc = false;
+      if (act && tok_ok) {
+        p = ex2((lp - sm.rowM[i]) * c) / sm.rowZ[i];
+        q = PROBS ? qp : ex2((lq - sm.rowM[G1 + i]) * c) / sm.rowZ[G1 + i];
+        acc = ui * q < p;
+      }
+      for (int r = lane; r < nrows; r += 32) {
+        const float Z = sm.rowZ[r];
+        nf |= !(Z > 0.f && Z <= 3.0e38f);
+      }
+      if (PROBS) nf |= act && tok_ok && !isfinite(q);
+      const unsigned am = __ballot_sync(0xffffffffu, acc) & gmask;
+      const unsigned badtok = __ballot_sync(0xffffffffu, act && !tok_ok);
+      const unsigned nfm = __ballot_sync(0xffffffffu, nf);
+      j = (~am & gmask) ? __ffs(~am & gmask) - 1 : g;
+      status = (badtok ? SV_ROW_BAD_TOKEN : 0) | (nfm ? SV_ROW_NONFINITE : 0);
+      if (h == 0 && act && P.out_diag) {
+        const float ap = (q > 0.f) ? fminf(1.f, p / q) : (p > 0.f ? 1.f : 0.f);
+        reinterpret_cast<float4 *>(P.out_diag)[(size_t)b * g + i] = make_float4(p, q, ap, 0.f);
+      }
+    }
+    // a stats kernel that could not finish its claims leaves partials unset
+    if (__ldcg(P.claim + kClaimStripes * kClaimStride)) status = SV_ROW_TIMEOUT;
+    if (lane == 0) { sm.j = j; sm.status = status; }
+  }
+  __syncthreads();
+  const int j = sm.j, status = sm.status;
+  // 3. rows finished by CTA 0 alone: invalid, greedy, bonus
+  const bool sweep = !status && !greedy && j < g;
+  if (!sweep) {
+    if (h != 0 || warp != 0) return;
+    if (status) {
+      pass_error_row(P, b, status, G1, ot, nullptr);
+      return;
+    }
+    int tok_j = 0;
+    if (greedy) {
+      tok_j = sm.rowI[j];
+    } else {
+      const float2 *pr = pb + (size_t)g * P.cMax;
+      tok_j = warp_sample_softmax_row<TDT>(tgt + (size_t)g * V, pr, P.cT, V, sm.rowM[g], c,
+                                           __ldg(P.unif + (size_t)b * G1 + g));
+    }
+    for (int s = lane; s < G1; s += 32)
+      ot[s] = s < j ? __ldg(P.draft_tokens + (size_t)b * g + s) : (s == j ? tok_j : -1);
+    if (lane == 0) {
+      P.out_nacc[b] = j;
+      if (P.out_status) P.out_status[b] = 0;
+    }
+    return;
+  }
+  // 4. residual sweep of the row pair (p_j, q_j), chunks [c0, c1) of this CTA
+  using PC = PairChunk<TDT, DDT>;
+  ResidCoef rk;
+  rk.c = c;
+  rk.ap = -fmaf(sm.rowM[j], c, log2f(sm.rowZ[j]));
+  rk.aq = PROBS ? 0.f : -fmaf(sm.rowM[G1 + j], c, log2f(sm.rowZ[G1 + j]));
+  const float Mp = sm.rowM[j];
+  const TT *prow = tgt + (size_t)j * V;
+  const DTy *qrow = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V;
+  float *rs = P.resid + (size_t)b * P.cR;
+  const int c0 = (int)((long long)h * P.cR / P.H), c1 = (int)((long long)(h + 1) * P.cR / P.H);
+  // each warp takes chunks c0 + warp, c0 + warp + 8, ..., two per step with
+  // every load of both in flight before the first residual term
+  for (int ch = c0 + warp; ch < c1; ch += 2 * kPassWarps) {
+    const int chb = ch + kPassWarps;
+    RawVec<TDT, PC::kVec> ra[2][PC::kVecs];
+    RawVec<DDT, PC::kVec> rq[2][PC::kVecs];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const int cc = w ? chb : ch;
+      const int x0 = cc * PC::kElems;
+      const int n = cc < c1 ? min(PC::kElems, V - x0) : 0;
+#pragma unroll
+      for (int u = 0; u < PC::kVecs; ++u) {
+        const int e = (lane + 32 * u) * PC::kVec;
+        if (e < n) {
+          ra[w][u].load(prow + x0 + e);
+          rq[w][u].load(qrow + x0 + e);
+        }
+      }
+    }
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+      const int cc = w ? chb : ch;
+      const int x0 = cc * PC::kElems;
+      const int n = cc < c1 ? min(PC::kElems, V - x0) : 0;
+      float s = 0.f;
+#pragma unroll
+      for (int u = 0; u < PC::kVecs; ++u) {
+        const int e = (lane + 32 * u) * PC::kVec;
+        if (e < n) {
+          float a[PC::kVec], q[PC::kVec];
+          ra[w][u].unpack(a);
+          rq[w][u].unpack(q);
+#pragma unroll
+          for (int t = 0; t < PC::kVec; ++t) s += resid_term<PROBS>(a[t], q[t], rk);
+        }
+      }
+      s = warp_sum(s);
+      if (lane == 0 && cc < c1) rs[cc] = s;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(P.done + b, 1u);
+    sm.last = (prev == (unsigned)P.H - 1u);
+    if (sm.last) __threadfence();
+  }
+  __syncthreads();
+  if (!sm.last || warp != 0) return;
+  // 5. the last CTA: crossing chunk of u * R, then a rescan of that chunk
+  const float u = __ldg(P.unif + (size_t)b * G1 + g);
+  float R = 0.f, base = 0.f;
+  const int t = warp_chunk_cross(P.cR, [&](int k) { return __ldcg(rs + k); }, u, R, base);
+  if (isnan(R) || isinf(R)) {
+    pass_error_row(P, b, SV_ROW_NONFINITE, G1, ot, nullptr);
+    return;
+  }
+  int k;
+  if (!(R > 0.f)) {
+    // no residual mass (p_j == q_j up to rounding): draw from p_j
+    k = warp_sample_softmax_row<TDT>(prow, pb + (size_t)j * P.cMax, P.cT, V, Mp, c, u);
+  } else {
+    const float target = u * R;
+    const int x0 = t * PC::kElems;
+    const int n = min(PC::kElems, V - x0);
+    float a[PC::kPer], qv[PC::kPer];
+    lane_consecutive_load<TDT, PC::kPer>(prow + x0, n, -CUDART_INF_F, a);
+    lane_consecutive_load<DDT, PC::kPer>(qrow + x0, n, PROBS ? 0.f : -CUDART_INF_F, qv);
+#pragma unroll
+    for (int e = 0; e < PC::kPer; ++e) a[e] = resid_term<PROBS>(a[e], qv[e], rk);
+    k = x0 + warp_rescan<PC::kPer>(a, base, target);
+  }
+  for (int s = lane; s < G1; s += 32)
+    ot[s] = s < j ? __ldg(P.draft_tokens + (size_t)b * g + s) : (s == j ? k : -1);
+  if (lane == 0) {
+    P.out_nacc[b] = j;
+    if (P.out_status) P.out_status[b] = 0;
+    if (P.out_diag) P.out_diag[((size_t)b * g + j) * 4 + 3] = R;
+  }
+}
+
+// One tree per CTA: argmax of every node row, validation, then the walk.
+template <int DT>
+__device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
+  const int N = P.N, V = P.V, D = P.max_depth;
+  const int lane = lane_id(), warp = warp_id();
+  if (threadIdx.x == 0) sm.flags = 0;
+  __syncthreads();
+  int flags = 0;
+  const float2 *pb = P.part + (size_t)b * N * P.cMax;
+  for (int r = warp; r < N; r += kPassWarps) {
+    const float2 mi = warp_row_argmax(pb + (size_t)r * P.cMax, P.cT);
+    if (lane == 0) sm.a[r] = __float_as_int(mi.y);
+    if (isnan(mi.x)) flags |= SV_ROW_NONFINITE;
+  }
+  for (int n = threadIdx.x; n < N; n += kPassThreads) {
+    const int par = __ldg(P.parent + (size_t)b * N + n);
+    const int tok = __ldg(P.node_tokens + (size_t)b * N + n);
+    sm.par[n] = par;
+    sm.tok[n] = tok;
+    if (n == 0 ? par != -1 : (par < 0 || par >= n)) flags |= SV_ROW_BAD_TREE;
+    if (n > 0 && (tok < 0 || tok >= V)) flags |= SV_ROW_BAD_TOKEN;
+  }
+  if (threadIdx.x == 0 && __ldcg(P.claim + kClaimStripes * kClaimStride)) flags |= SV_ROW_TIMEOUT;
+  if (flags) atomicOr(&sm.flags, flags);
+  __syncthreads();
+  if (warp != 0) return;
+  flags = sm.flags;
+  const int W = D + 1;
+  int32_t *op = P.out_path + (size_t)b * W;
+  int32_t *ot = P.out_tokens + (size_t)b * W;
+  if (flags) {
+    pass_error_row(P, b, flags, W, ot, op);
+    return;
+  }
+  int cur = 0, d = 0;
+  while (d < D) {
+    const int a = sm.a[cur];
+    int found = -1;
+    for (int base = cur + 1; base < N && found < 0; base += 32) {
+      const int ci = base + lane;
+      const bool m = ci < N && sm.par[ci] == cur && sm.tok[ci] == a;
+      const unsigned bm = __ballot_sync(0xffffffffu, m);
+      if (bm) found = base + __ffs(bm) - 1;
+    }
+    if (found < 0) break;
+    if (lane == 0) sm.path[d] = found;
+    cur = found;
+    ++d;
+  }
+  __syncwarp();
+  if (lane < W) {
+    op[lane] = lane < d ? sm.path[lane] : -1;
+    ot[lane] = lane < d ? sm.tok[sm.path[lane]] : (lane == d ? sm.a[cur] : -1);
+  }
+  if (lane == 0) {
+    P.out_nacc[b] = d;
+    if (P.out_status) P.out_status[b] = 0;
+  }
+}
+
+template <int MODE, int TDT, int DDT, bool PROBS>
+__global__ void __launch_bounds__(kPassThreads, 2) sv_decide_kernel(const PassParams P) {
+  grid_dependency_wait();  // the stats kernel's partials and counters are complete
+  const int b = blockIdx.x / P.H, h = blockIdx.x - b * P.H;
+  if (MODE == MODE_TREE) {
+    __shared__ TreeSmem sm;
+    decide_tree<TDT>(P, b, sm);
+  } else {
+    __shared__ DecideSmem sm;
+    decide_chain_row<MODE, TDT, DDT, PROBS>(P, b, h, sm);
+  }
+}
+
+}  // namespace sv

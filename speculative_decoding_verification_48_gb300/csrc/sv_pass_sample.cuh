@@ -1,0 +1,199 @@
+// Inverse-CDF draws for the decide kernel: crossing search over chunk masses
+// and rescan of the crossing chunk ("論文解説: Speculative Sampling",
+// §修正付き棄却サンプリング; the draw is the inverse CDF in ascending vocabulary
+// order: the smallest k with sum_{x<=k} w(x) > u * sum_x w(x)).
+#pragma once
+
+#include "sv_pass_common.cuh"
+
+namespace sv {
+
+// First index i in [0, cnt) where the running sum of w(i) exceeds target;
+// `base` receives the sum before it.  If rounding leaves no such i, the last
+// i with w(i) > 0 (and the sum before it); -1 if every w is zero.
+template <class WF>
+__device__ __forceinline__ int warp_prefix_cross(int cnt, float target, WF w, float &base) {
+  const int lane = lane_id();
+  float acc = 0.f, last_base = 0.f;
+  int last_i = -1;
+  for (int c0 = 0; c0 < cnt; c0 += 32) {
+    const int i = c0 + lane;
+    const float v = i < cnt ? w(i) : 0.f;
+    float incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, acc + incl > target);
+    const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      base = acc + __shfl_sync(0xffffffffu, incl - v, l);
+      return c0 + l;
+    }
+    if (pos) {
+      const int l = 31 - __clz(pos);
+      last_base = acc + __shfl_sync(0xffffffffu, incl - v, l);
+      last_i = c0 + l;
+    }
+    acc += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  base = last_base;
+  return last_i;
+}
+
+// The lane's PER consecutive elements [lane * PER, lane * PER + PER) of a
+// chunk starting at `base` (16-byte aligned); slots at or past n get `pad`.
+template <int DT, int PER>
+__device__ __forceinline__ void lane_consecutive_load(const typename Elt<DT>::T *base, int n,
+                                                      float pad, float (&v)[PER]) {
+  using E = Elt<DT>;
+  constexpr int VEC = E::kVec;
+  const int e0 = lane_id() * PER;
+  const typename E::T *p = base + e0;
+  if (e0 + PER <= n) {
+    if constexpr (PER % VEC == 0) {
+#pragma unroll
+      for (int k = 0; k < PER / VEC; ++k) E::unpack(ld_nc16(p + k * VEC), &v[k * VEC]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < PER; ++k) v[k] = E::load1(p + k);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < PER; ++k) v[k] = (e0 + k < n) ? E::load1(p + k) : pad;
+  }
+}
+
+// Crossing inside a chunk whose lane-consecutive weights are w[PER]: the
+// local index of the first element where base + cumsum > target, or the last
+// positive element if rounding leaves none.
+template <int PER>
+__device__ __forceinline__ int warp_rescan(const float (&w)[PER], float base, float target) {
+  const int lane = lane_id();
+  float tsum = 0.f;
+  int lastpos = -1;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    tsum += w[k];
+    if (w[k] > 0.f) lastpos = lane * PER + k;
+  }
+  float incl = tsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const float start = base + incl - tsum;
+  const unsigned hit = __ballot_sync(0xffffffffu, start + tsum > target);
+  const int last_any = warp_max_int(lastpos);
+  if (!hit) return last_any < 0 ? 0 : last_any;
+  const int l = __ffs(hit) - 1;
+  int k = -1;
+  float acc = start;
+#pragma unroll
+  for (int kk = 0; kk < PER; ++kk) {
+    acc += w[kk];
+    if (k < 0 && acc > target) k = lane * PER + kk;
+  }
+  if (k < 0) k = lastpos >= 0 ? lastpos : lane * PER;
+  return __shfl_sync(0xffffffffu, k, l);
+}
+
+// Up to 32 K per-chunk weights held in registers: w[k] is the weight of
+// index 32 k + lane (0 past cnt).  One round trip loads them all.
+constexpr int kRegK = 16;
+
+template <class WF>
+__device__ __forceinline__ void warp_load_weights(int cnt, WF wf, float (&w)[kRegK]) {
+  const int lane = lane_id();
+#pragma unroll
+  for (int k = 0; k < kRegK; ++k) {
+    const int i = 32 * k + lane;
+    w[k] = i < cnt ? wf(i) : 0.f;
+  }
+}
+
+// warp_prefix_cross over register-held weights (cnt <= 32 kRegK).
+__device__ __forceinline__ int warp_cross_regs(const float (&w)[kRegK], int cnt, float target,
+                                               float &base) {
+  const int lane = lane_id();
+  float acc = 0.f, last_base = 0.f;
+  int last_i = -1;
+#pragma unroll
+  for (int k = 0; k < kRegK; ++k) {
+    if (32 * k < cnt) {
+      const float v = w[k];
+      float incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, acc + incl > target);
+      const unsigned pos = __ballot_sync(0xffffffffu, v > 0.f);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        base = acc + __shfl_sync(0xffffffffu, incl - v, l);
+        return 32 * k + l;
+      }
+      if (pos) {
+        const int l = 31 - __clz(pos);
+        last_base = acc + __shfl_sync(0xffffffffu, incl - v, l);
+        last_i = 32 * k + l;
+      }
+      acc += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  base = last_base;
+  return last_i;
+}
+
+// Crossing of u * R over per-chunk weights wf(i), i < cnt, R = their sum
+// (returned in R): register-held when they fit (one round trip), else
+// streamed 32 at a time.  Returns the chunk (>= 0) and the sum before it.
+template <class WF>
+__device__ __forceinline__ int warp_chunk_cross(int cnt, WF wf, float u, float &R, float &base) {
+  int t;
+  if (cnt <= 32 * kRegK) {
+    float w[kRegK];
+    warp_load_weights(cnt, wf, w);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRegK; ++k) s += w[k];
+    R = warp_sum(s);
+    t = warp_cross_regs(w, cnt, u * R, base);
+  } else {
+    float s = 0.f;
+    for (int i = lane_id(); i < cnt; i += 32) s += wf(i);
+    R = warp_sum(s);
+    t = warp_prefix_cross(cnt, u * R, wf, base);
+  }
+  return t < 0 ? 0 : t;
+}
+
+// Draw from softmax row `row` (V elements of DT, max M, scale c) with the
+// stats kernel's chunk partials part[cnt]: the chunk masses
+// s_i 2^((m_i - M) c) locate the crossing chunk of u * R, then that chunk is
+// rescanned element by element.  Returns a vocabulary index.
+template <int DT>
+__device__ int warp_sample_softmax_row(const typename Elt<DT>::T *row, const float2 *part, int cnt,
+                                       int V, float M, float c, float u) {
+  using C = Chunk<DT>;
+  auto wt = [&](int i) {
+    const float2 p = __ldcg(part + i);
+    return p.x != -CUDART_INF_F ? p.y * ex2((p.x - M) * c) : 0.f;
+  };
+  float R = 0.f, base = 0.f;
+  const int t = warp_chunk_cross(cnt, wt, u, R, base);
+  const int x0 = t * C::kElems;
+  const int n = min(C::kElems, V - x0);
+  float v[C::kPer];
+  lane_consecutive_load<DT, C::kPer>(row + x0, n, -CUDART_INF_F, v);
+#pragma unroll
+  for (int k = 0; k < C::kPer; ++k) v[k] = ex2((v[k] - M) * c);
+  return x0 + warp_rescan<C::kPer>(v, base, u * R);
+}
+
+}  // namespace sv

@@ -1,0 +1,286 @@
+// Row statistics pass: every logit row the verification needs is read once
+// from HBM and reduced to warp-chunk partials.
+//
+// Softmax rows ("論文解説: Speculative Sampling", §実装のポイント: both models'
+// rows go through softmax(logits / T)): (m, s) with m the chunk maximum and
+// s = sum_x 2^(x c - m c), c = log2(e) / T.  Argmax rows (greedy rows,
+// "投機的デコーディングとは？" §ドラフト生成と並列検証の仕組み, and tree nodes, SpecInfer
+// explainer §推論方法): (max value, lowest index holding it).
+//
+// Work is a list of warp-chunks that warps claim one at a time from striped
+// counters (below), so the grid reads one contiguous front of memory and
+// fast warps take more chunks than slow ones.
+// Each warp keeps the next chunk's four 16-byte loads per lane in flight
+// while it reduces the current one.  For chains the list runs from the last
+// draft position to the first: the rows that the residual sweep is most
+// likely to re-read (early positions, where the first rejection usually
+// falls) are then the most recently read when the sweep starts, and still in
+// L2.  Warp-chunks a row does not need (draft rows of greedy rows, every row
+// of a row with an invalid temperature) cost nothing.
+#pragma once
+
+#include "sv_pass_sample.cuh"
+
+namespace sv {
+
+enum ChunkKind { CK_SKIP = 0, CK_SOFTMAX = 1, CK_ARGMAX = 2 };
+
+struct ChunkRef {
+  const void *src;  // first byte of the warp-chunk
+  float2 *dst;      // its partial
+  int kind, n, x0;  // n valid elements, x0 = first vocabulary index
+  int draft;        // 1: element type DDT, else TDT
+  float c;
+};
+
+template <int MODE, int TDT, int DDT, bool PROBS>
+__device__ __forceinline__ ChunkRef decode_chunk(const PassParams &P, int k) {
+  ChunkRef r;
+  int b, row, ci, draft = 0, pos = 0;
+  if (MODE == MODE_TREE) {
+    const int gr = (int)fdiv((unsigned)k, P.fd_cT);  // global node row b * N + n
+    ci = k - gr * P.cT;
+    b = (int)fdiv((unsigned)gr, P.fd_N);
+    row = gr - b * P.N;
+  } else {
+    const int g = P.gamma;
+    const int cP = P.cT + P.cD;
+    const int head = P.B * P.cT;  // position gamma: target rows only
+    if (k < head) {
+      pos = g;
+      b = (int)fdiv((unsigned)k, P.fd_cT);
+      ci = k - b * P.cT;
+    } else {
+      const int k2 = k - head;
+      const int blk = (int)fdiv((unsigned)k2, P.fd_blk);
+      pos = g - 1 - blk;
+      const int r2 = k2 - blk * P.B * cP;
+      b = (int)fdiv((unsigned)r2, P.fd_cP);
+      const int t = r2 - b * cP;
+      draft = t >= P.cT;
+      ci = draft ? t - P.cT : t;
+    }
+    row = draft ? g + 1 + pos : pos;
+  }
+  const int E = draft ? Chunk<DDT>::kElems : Chunk<TDT>::kElems;
+  r.x0 = ci * E;
+  r.n = min(E, P.V - r.x0);
+  r.draft = draft;
+  r.dst = P.part + ((size_t)b * P.rows + row) * P.cMax + ci;
+  r.c = 0.f;
+  if (MODE == MODE_CHAIN) {
+    const float T = __ldg(P.temps + b);
+    if (bad_temperature(T)) r.kind = CK_SKIP;
+    else if (T > 0.f) { r.kind = CK_SOFTMAX; r.c = kLog2e / T; }
+    else r.kind = draft ? CK_SKIP : CK_ARGMAX;
+  } else {
+    r.kind = CK_ARGMAX;
+  }
+  if (draft) {
+    const auto *d = reinterpret_cast<const typename Elt<DDT>::T *>(P.draft);
+    r.src = d + ((size_t)b * P.gamma + pos) * P.V + r.x0;
+  } else {
+    const auto *t = reinterpret_cast<const typename Elt<TDT>::T *>(P.target);
+    const int rows_per = (MODE == MODE_TREE) ? P.N : P.gamma + 1;
+    r.src = t + ((size_t)b * rows_per + row) * P.V + r.x0;
+  }
+  return r;
+}
+
+// Packed -inf of one 32-bit word of each element type.
+template <int DT> __device__ __forceinline__ unsigned neg_inf_word() {
+  return DT == SV_F32 ? 0xff800000u : (DT == SV_BF16 ? 0xff80ff80u : 0xfc00fc00u);
+}
+
+// The lane's four 16-byte vectors of a warp-chunk: vector l + 32 u holds
+// bytes [16 (l + 32 u), 16 (l + 32 u) + 16) of the chunk.  Vectors past the
+// row end (n is a multiple of the vector width on this path) are filled
+// with -inf instead of loaded.
+template <int DT>
+__device__ __forceinline__ void chunk_issue_t(const ChunkRef &r, uint4 (&buf)[kChunkVecs]) {
+  constexpr int VEC = Chunk<DT>::kVec, ES = Chunk<DT>::kEs;
+  const int lane = lane_id();
+  const unsigned ni = neg_inf_word<DT>();
+#pragma unroll
+  for (int u = 0; u < kChunkVecs; ++u) {
+    const int e = (lane + 32 * u) * VEC;
+    if (e < r.n) buf[u] = ld_nc16(static_cast<const char *>(r.src) + (size_t)e * ES);
+    else buf[u] = make_uint4(ni, ni, ni, ni);
+  }
+}
+
+template <int TDT, int DDT>
+__device__ __forceinline__ void chunk_issue(const ChunkRef &r, uint4 (&buf)[kChunkVecs]) {
+  if (r.kind == CK_SKIP) return;
+  if (TDT == DDT || !r.draft) chunk_issue_t<TDT>(r, buf);
+  else chunk_issue_t<DDT>(r, buf);
+}
+
+// NaN-propagating max of two packed words (2 x bf16, 2 x f16 or 1 x f32).
+template <int DT> __device__ __forceinline__ unsigned packed_max(unsigned a, unsigned b) {
+  unsigned d;
+  if constexpr (DT == SV_BF16) asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else if constexpr (DT == SV_F16) asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  else asm("max.NaN.f32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// The larger of the elements in a packed word, as f32 (NaN if either is).
+template <int DT> __device__ __forceinline__ float packed_word_max(unsigned w) {
+  if constexpr (DT == SV_F32) {
+    return __uint_as_float(w);
+  } else {
+    float lo, hi;
+    if constexpr (DT == SV_BF16) {
+      lo = __uint_as_float(w << 16);
+      hi = __uint_as_float(w & 0xffff0000u);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+      lo = f.x;
+      hi = f.y;
+    }
+    return max_nan(lo, hi);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void chunk_reduce(const ChunkRef &r, const uint4 (&buf)[kChunkVecs]) {
+  using C = Chunk<DT>;
+  constexpr int VEC = C::kVec;
+  const int lane = lane_id();
+  // chunk maximum on packed words
+  unsigned mw0 = packed_max<DT>(buf[0].x, buf[0].y), mw1 = packed_max<DT>(buf[0].z, buf[0].w);
+#pragma unroll
+  for (int u = 1; u < kChunkVecs; ++u) {
+    mw0 = packed_max<DT>(mw0, packed_max<DT>(buf[u].x, buf[u].y));
+    mw1 = packed_max<DT>(mw1, packed_max<DT>(buf[u].z, buf[u].w));
+  }
+  const float m = warp_max_nan(packed_word_max<DT>(packed_max<DT>(mw0, mw1)));
+  float2 out;
+  if (r.kind == CK_SOFTMAX) {
+    // s = sum 2^(x c - m c).  The exponent is one FFMA against mc = RN(m c);
+    // that scales every term by 2^d, d = m c - mc (exact by FMA), which is
+    // divided out once.  A huge |m c| (tiny T) or a non-finite m falls back
+    // to (x - m) c, which also turns +inf / NaN into a NaN sum.
+    const float c = r.c;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+    float scale = 1.f;
+    if (m != -CUDART_INF_F) {
+      const float mc = m * c;
+      if (fabsf(mc) <= 1.0e37f) {
+        const float d = fmaf(m, c, -mc);
+#pragma unroll
+        for (int u = 0; u < kChunkVecs; ++u) {
+          float v[VEC];
+          Elt<DT>::unpack(buf[u], v);
+#pragma unroll
+          for (int t = 0; t < VEC; ++t) s4[t & 3] += ex2(fmaf(v[t], c, -mc));
+        }
+        scale = ex2(-d);
+      } else {
+#pragma unroll
+        for (int u = 0; u < kChunkVecs; ++u) {
+          float v[VEC];
+          Elt<DT>::unpack(buf[u], v);
+#pragma unroll
+          for (int t = 0; t < VEC; ++t) s4[t & 3] += ex2((v[t] - m) * c);
+        }
+      }
+    }
+    out = make_float2(m, warp_sum((s4[0] + s4[1]) + (s4[2] + s4[3])) * scale);
+  } else {
+    int idx = 0x7fffffff;
+#pragma unroll
+    for (int u = kChunkVecs - 1; u >= 0; --u) {
+      float v[VEC];
+      Elt<DT>::unpack(buf[u], v);
+#pragma unroll
+      for (int t = VEC - 1; t >= 0; --t)
+        if (v[t] == m) idx = (lane + 32 * u) * VEC + t;  // descending: keeps the lowest
+    }
+    idx = warp_min_int(idx);
+    out = make_float2(m, __int_as_float(idx == 0x7fffffff ? idx : r.x0 + idx));
+  }
+  if (lane == 0) *r.dst = out;
+}
+
+template <int MODE, int TDT, int DDT, bool PROBS>
+__device__ __forceinline__ void chunk_process(const ChunkRef &r, const uint4 (&buf)[kChunkVecs]) {
+  if (r.kind == CK_SKIP) return;
+  if (TDT == DDT || !r.draft) chunk_reduce<TDT>(r, buf);
+  else chunk_reduce<DDT>(r, buf);
+}
+
+// Dynamic work claims: kClaimStripes counters, counter s handing out the
+// chunks k = kClaimStripes * i + s in order, so all stripes advance through
+// the list together (one contiguous front in memory, the list order kept)
+// while no single address takes every atomic.  A warp starts on stripe
+// (warp index mod kClaimStripes); when its stripe runs dry it reads every
+// counter at once and moves to a stripe with chunks left.  Returns -1 once
+// every stripe is exhausted.
+struct Claimer {
+  int s;
+};
+
+__device__ __forceinline__ unsigned claim_issue(const PassParams &P, const Claimer &c) {
+  unsigned v = 0;
+  if (lane_id() == 0) v = atomicAdd(P.claim + c.s * kClaimStride, 1u);
+  return v;
+}
+
+__device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, unsigned pend) {
+  const int lane = lane_id();
+  long long k = (long long)__shfl_sync(0xffffffffu, pend, 0) * kClaimStripes + c.s;
+  // every probe finds a stripe with chunks left or ends the loop; a claim
+  // lost to a race only repeats the probe, so the bound is never reached in
+  // practice — if it were, the call is flagged rather than left unfinished
+  for (int probe = 0; k >= P.total; ++probe) {
+    if (probe == kClaimProbes) {
+      if (lane == 0) atomicOr(P.claim + kClaimStripes * kClaimStride, 1u);
+      return -1;
+    }
+    unsigned cnt = 0xffffffffu;
+    if (lane < kClaimStripes) cnt = ld_volatile_u32(P.claim + lane * kClaimStride);
+    const bool has = lane < kClaimStripes && (long long)cnt * kClaimStripes + lane < P.total;
+    const unsigned m = __ballot_sync(0xffffffffu, has);
+    if (!m) return -1;
+    c.s = __ffs(m) - 1;
+    k = (long long)__shfl_sync(0xffffffffu, claim_issue(P, c), 0) * kClaimStripes + c.s;
+  }
+  return (int)k;
+}
+
+template <int MODE, int TDT, int DDT, bool PROBS>
+__global__ void __launch_bounds__(kPassThreads, 3) sv_stats_kernel(const PassParams P) {
+  Claimer cl{(int)((blockIdx.x * kPassWarps + warp_id()) % kClaimStripes)};
+  uint4 b0[kChunkVecs], b1[kChunkVecs];
+  int ka = claim_resolve(P, cl, claim_issue(P, cl));
+  if (ka >= 0) {
+    ChunkRef ra = decode_chunk<MODE, TDT, DDT, PROBS>(P, ka);
+    chunk_issue<TDT, DDT>(ra, b0);
+    unsigned pend = claim_issue(P, cl);  // the next claim is in flight while a chunk is reduced
+    // two chunks per iteration so both buffers have static names
+    while (true) {
+      const int kb = claim_resolve(P, cl, pend);
+      ChunkRef rb;
+      rb.kind = CK_SKIP;
+      if (kb >= 0) {
+        rb = decode_chunk<MODE, TDT, DDT, PROBS>(P, kb);
+        chunk_issue<TDT, DDT>(rb, b1);
+        pend = claim_issue(P, cl);
+      }
+      chunk_process<MODE, TDT, DDT, PROBS>(ra, b0);
+      if (kb < 0) break;
+      ka = claim_resolve(P, cl, pend);
+      if (ka >= 0) {
+        ra = decode_chunk<MODE, TDT, DDT, PROBS>(P, ka);
+        chunk_issue<TDT, DDT>(ra, b0);
+        pend = claim_issue(P, cl);
+      }
+      chunk_process<MODE, TDT, DDT, PROBS>(rb, b1);
+      if (ka < 0) break;
+    }
+  }
+  grid_dependents_launch();
+}
+
+}  // namespace sv
