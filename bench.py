@@ -42,12 +42,13 @@ from speculative_decoding_verification_48_gb300 import workloads as W  # noqa: E
 
 METRIC = "verified draft positions/sec and achieved HBM GB/s vs 8 TB/s (1 GB300)"
 # Rows of every bench workload start on 16-byte boundaries, so each call runs
-# the streaming kernel (one launch after the control-block memset) unless
+# the two-launch path (sv_stats_kernel, then sv_decide_kernel as its
+# programmatic dependent, after a control-block memset) unless
 # SPEC_VERIFY_KERNEL=tile selects the register-tile kernels (two launches).
 _TILE = os.environ.get("SPEC_VERIFY_KERNEL", "").startswith("t")
 KERNEL_NAME = ("sv_verify_kernel (Phase-A + Phase-B launches)" if _TILE
-               else "sv_stream_kernel (one persistent launch)")
-LAUNCHES_PER_CALL = 2 if _TILE else 1
+               else "sv_stats_kernel + sv_decide_kernel (one call)")
+LAUNCHES_PER_CALL = 2
 UNIT = "positions/s"
 
 

@@ -3,7 +3,7 @@
 // loads and warp-level merge / crossing helpers.
 //
 //   sv_stats_kernel   streams every logit row once.  Each warp reduces
-//                     "warp-chunks" of 2 KB (32 lanes x 4 x 16-byte vectors)
+//                     "warp-chunks" of 4 KB (32 lanes x 8 x 16-byte vectors)
 //                     to a partial — (max, sum exp2) for a softmax row,
 //                     (max, first index) for an argmax row — and stores it.
 //                     Warps are independent: no block barrier, no atomics.
@@ -21,8 +21,9 @@ namespace sv {
 
 constexpr int kPassThreads = 256;
 constexpr int kPassWarps = kPassThreads / 32;
-constexpr int kChunkBytes = 2048;  // one warp-chunk
-constexpr int kChunkVecs = 4;      // 16-byte vectors per lane per warp-chunk
+constexpr int kChunkBytes = 4096;  // one warp-chunk of the stats kernel
+constexpr int kChunkVecs = 8;      // 16-byte vectors per lane per warp-chunk
+constexpr int kResidBytes = 2048;  // one residual chunk of a row pair
 constexpr int kClaimStripes = 16;  // stats-kernel claim counters
 constexpr int kClaimStride = 32;   // 128 bytes between counters
 constexpr int kClaimProbes = 4096; // bound of the end-of-work probe loop
@@ -37,7 +38,7 @@ template <int DT> struct Chunk {
 // Residual chunks of a row pair: 2 KB of the wider of the two element types.
 template <int TDT, int DDT> struct PairChunk {
   static constexpr int kEs = Chunk<TDT>::kEs > Chunk<DDT>::kEs ? Chunk<TDT>::kEs : Chunk<DDT>::kEs;
-  static constexpr int kElems = kChunkBytes / kEs;
+  static constexpr int kElems = kResidBytes / kEs;
   static constexpr int kVec = 16 / kEs;   // elements per vector, both rows
   static constexpr int kVecs = kElems / (32 * kVec);
   static constexpr int kPer = kElems / 32;
@@ -100,7 +101,7 @@ inline PassLayout make_pass_layout(int B, int rows, int V, int esT, int esD, boo
   L.cT = ceil_div(V, kChunkBytes / esT);
   L.cD = stream_draft ? ceil_div(V, kChunkBytes / esD) : 0;
   L.cMax = L.cT > L.cD ? L.cT : L.cD;
-  L.cR = ceil_div(V, kChunkBytes / (esT > esD ? esT : esD));
+  L.cR = ceil_div(V, kResidBytes / (esT > esD ? esT : esD));
   size_t off = 0;
   L.claim = off; off += (size_t)(kClaimStripes + 1) * kClaimStride * 4;
   L.done = off;  off = align_up(off + (size_t)B * 4, 256);

@@ -10,7 +10,7 @@
 // Work is a list of warp-chunks that warps claim one at a time from striped
 // counters (below), so the grid reads one contiguous front of memory and
 // fast warps take more chunks than slow ones.
-// Each warp keeps the next chunk's four 16-byte loads per lane in flight
+// Each warp keeps the next chunk's eight 16-byte loads per lane in flight
 // while it reduces the current one.  For chains the list runs from the last
 // draft position to the first: the rows that the residual sweep is most
 // likely to re-read (early positions, where the first rejection usually
@@ -92,7 +92,7 @@ template <int DT> __device__ __forceinline__ unsigned neg_inf_word() {
   return DT == SV_F32 ? 0xff800000u : (DT == SV_BF16 ? 0xff80ff80u : 0xfc00fc00u);
 }
 
-// The lane's four 16-byte vectors of a warp-chunk: vector l + 32 u holds
+// The lane's eight 16-byte vectors of a warp-chunk: vector l + 32 u holds
 // bytes [16 (l + 32 u), 16 (l + 32 u) + 16) of the chunk.  Vectors past the
 // row end (n is a multiple of the vector width on this path) are filled
 // with -inf instead of loaded.
@@ -148,13 +148,16 @@ __device__ __forceinline__ void chunk_reduce(const ChunkRef &r, const uint4 (&bu
   constexpr int VEC = C::kVec;
   const int lane = lane_id();
   // chunk maximum on packed words
-  unsigned mw0 = packed_max<DT>(buf[0].x, buf[0].y), mw1 = packed_max<DT>(buf[0].z, buf[0].w);
+  unsigned mw[4] = {buf[0].x, buf[0].y, buf[0].z, buf[0].w};
 #pragma unroll
   for (int u = 1; u < kChunkVecs; ++u) {
-    mw0 = packed_max<DT>(mw0, packed_max<DT>(buf[u].x, buf[u].y));
-    mw1 = packed_max<DT>(mw1, packed_max<DT>(buf[u].z, buf[u].w));
+    mw[0] = packed_max<DT>(mw[0], buf[u].x);
+    mw[1] = packed_max<DT>(mw[1], buf[u].y);
+    mw[2] = packed_max<DT>(mw[2], buf[u].z);
+    mw[3] = packed_max<DT>(mw[3], buf[u].w);
   }
-  const float m = warp_max_nan(packed_word_max<DT>(packed_max<DT>(mw0, mw1)));
+  const float m = warp_max_nan(
+      packed_word_max<DT>(packed_max<DT>(packed_max<DT>(mw[0], mw[1]), packed_max<DT>(mw[2], mw[3]))));
   float2 out;
   if (r.kind == CK_SOFTMAX) {
     // s = sum 2^(x c - m c).  The exponent is one FFMA against mc = RN(m c);
@@ -250,7 +253,10 @@ __device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, un
 }
 
 template <int MODE, int TDT, int DDT, bool PROBS>
-__global__ void __launch_bounds__(kPassThreads, 3) sv_stats_kernel(const PassParams P) {
+__global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassParams P) {
+  // The decide kernel may launch at once: its CTAs take the place of
+  // finished stats CTAs and wait on the device for this grid to complete.
+  grid_dependents_launch();
   Claimer cl{(int)((blockIdx.x * kPassWarps + warp_id()) % kClaimStripes)};
   uint4 b0[kChunkVecs], b1[kChunkVecs];
   int ka = claim_resolve(P, cl, claim_issue(P, cl));
@@ -280,7 +286,6 @@ __global__ void __launch_bounds__(kPassThreads, 3) sv_stats_kernel(const PassPar
       if (ka < 0) break;
     }
   }
-  grid_dependents_launch();
 }
 
 }  // namespace sv
