@@ -93,9 +93,9 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   S.cR = L.cR;
   int H = 1;
   if (MODE == MODE_CHAIN) {
-    // about 16 residual chunks per decide CTA (one step of two chunks per
-    // warp), while the decide grid stays within one wave of resident CTAs
-    H = (L.cR + 15) / 16;
+    // about 8 residual chunks per decide CTA (one per warp), while the
+    // decide grid stays within one wave of resident CTAs
+    H = (L.cR + kPassWarps - 1) / kPassWarps;
     const int cap = (occd * sms) / P0.B;
     if (H > cap) H = cap;
     if (H > 32) H = 32;

@@ -79,6 +79,8 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     }
   }
   grid_dependency_wait();
+  unsigned claim_err = 0;
+  if (warp == 0) claim_err = __ldcg(P.claim + kClaimStripes * kClaimStride);
   if (badT) {
     if (warp == 0) {
       pass_error_row(P, b, SV_ROW_BAD_TEMPERATURE, G1, ot, nullptr);
@@ -157,7 +159,7 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
       }
     }
     // a stats kernel that could not finish its claims leaves partials unset
-    if (__ldcg(P.claim + kClaimStripes * kClaimStride)) status = SV_ROW_TIMEOUT;
+    if (claim_err) status = SV_ROW_TIMEOUT;
     if (lane == 0) { sm.j = j; sm.status = status; }
   }
   __syncthreads();
@@ -197,46 +199,35 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   const DTy *qrow = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V;
   float *rs = P.resid + (size_t)b * P.cR;
   const int c0 = (int)((long long)h * P.cR / P.H), c1 = (int)((long long)(h + 1) * P.cR / P.H);
-  // each warp takes chunks c0 + warp, c0 + warp + 8, ..., two per step with
-  // every load of both in flight before the first residual term
-  for (int ch = c0 + warp; ch < c1; ch += 2 * kPassWarps) {
-    const int chb = ch + kPassWarps;
-    RawVec<TDT, PC::kVec> ra[2][PC::kVecs];
-    RawVec<DDT, PC::kVec> rq[2][PC::kVecs];
+  // each warp takes chunks c0 + warp, c0 + warp + 8, ..., with all loads of
+  // a chunk in flight before its first residual term
+  for (int ch = c0 + warp; ch < c1; ch += kPassWarps) {
+    const int x0 = ch * PC::kElems;
+    const int n = min(PC::kElems, V - x0);
+    RawVec<TDT, PC::kVec> ra[PC::kVecs];
+    RawVec<DDT, PC::kVec> rq[PC::kVecs];
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const int cc = w ? chb : ch;
-      const int x0 = cc * PC::kElems;
-      const int n = cc < c1 ? min(PC::kElems, V - x0) : 0;
-#pragma unroll
-      for (int u = 0; u < PC::kVecs; ++u) {
-        const int e = (lane + 32 * u) * PC::kVec;
-        if (e < n) {
-          ra[w][u].load(prow + x0 + e);
-          rq[w][u].load(qrow + x0 + e);
-        }
+    for (int u = 0; u < PC::kVecs; ++u) {
+      const int e = (lane + 32 * u) * PC::kVec;
+      if (e < n) {
+        ra[u].load(prow + x0 + e);
+        rq[u].load(qrow + x0 + e);
       }
     }
+    float s = 0.f;
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
-      const int cc = w ? chb : ch;
-      const int x0 = cc * PC::kElems;
-      const int n = cc < c1 ? min(PC::kElems, V - x0) : 0;
-      float s = 0.f;
+    for (int u = 0; u < PC::kVecs; ++u) {
+      const int e = (lane + 32 * u) * PC::kVec;
+      if (e < n) {
+        float a[PC::kVec], q[PC::kVec];
+        ra[u].unpack(a);
+        rq[u].unpack(q);
 #pragma unroll
-      for (int u = 0; u < PC::kVecs; ++u) {
-        const int e = (lane + 32 * u) * PC::kVec;
-        if (e < n) {
-          float a[PC::kVec], q[PC::kVec];
-          ra[w][u].unpack(a);
-          rq[w][u].unpack(q);
-#pragma unroll
-          for (int t = 0; t < PC::kVec; ++t) s += resid_term<PROBS>(a[t], q[t], rk);
-        }
+        for (int t = 0; t < PC::kVec; ++t) s += resid_term<PROBS>(a[t], q[t], rk);
       }
-      s = warp_sum(s);
-      if (lane == 0 && cc < c1) rs[cc] = s;
     }
+    s = warp_sum(s);
+    if (lane == 0) rs[ch] = s;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -340,7 +331,7 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
 }
 
 template <int MODE, int TDT, int DDT, bool PROBS>
-__global__ void __launch_bounds__(kPassThreads, 2) sv_decide_kernel(const PassParams P) {
+__global__ void __launch_bounds__(kPassThreads, 4) sv_decide_kernel(const PassParams P) {
   grid_dependency_wait();  // the stats kernel's partials and counters are complete
   const int b = blockIdx.x / P.H, h = blockIdx.x - b * P.H;
   if (MODE == MODE_TREE) {

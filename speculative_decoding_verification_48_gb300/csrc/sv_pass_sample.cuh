@@ -181,19 +181,33 @@ template <int DT>
 __device__ int warp_sample_softmax_row(const typename Elt<DT>::T *row, const float2 *part, int cnt,
                                        int V, float M, float c, float u) {
   using C = Chunk<DT>;
+  constexpr int HALF = C::kElems / 2, PER = HALF / 32;
   auto wt = [&](int i) {
     const float2 p = __ldcg(part + i);
     return p.x != -CUDART_INF_F ? p.y * ex2((p.x - M) * c) : 0.f;
   };
   float R = 0.f, base = 0.f;
   const int t = warp_chunk_cross(cnt, wt, u, R, base);
-  const int x0 = t * C::kElems;
-  const int n = min(C::kElems, V - x0);
-  float v[C::kPer];
-  lane_consecutive_load<DT, C::kPer>(row + x0, n, -CUDART_INF_F, v);
+  const float target = u * R;
+  // rescan the crossing chunk one half at a time (32 values per lane)
+  int x0 = t * C::kElems;
+  float v[PER];
+  lane_consecutive_load<DT, PER>(row + x0, min(HALF, V - x0), -CUDART_INF_F, v);
+  float hs = 0.f;
 #pragma unroll
-  for (int k = 0; k < C::kPer; ++k) v[k] = ex2((v[k] - M) * c);
-  return x0 + warp_rescan<C::kPer>(v, base, u * R);
+  for (int k = 0; k < PER; ++k) {
+    v[k] = ex2((v[k] - M) * c);
+    hs += v[k];
+  }
+  hs = warp_sum(hs);
+  if (base + hs <= target && x0 + HALF < V) {
+    base += hs;
+    x0 += HALF;
+    lane_consecutive_load<DT, PER>(row + x0, min(HALF, V - x0), -CUDART_INF_F, v);
+#pragma unroll
+    for (int k = 0; k < PER; ++k) v[k] = ex2((v[k] - M) * c);
+  }
+  return x0 + warp_rescan<PER>(v, base, target);
 }
 
 }  // namespace sv
