@@ -13,10 +13,10 @@ measured copy bandwidth in MEASURED_PEAKS.json.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload c3|c5|c2|c1] [--quick]
 
-Under torchrun (N > 1) every rank verifies its own batch (rows r*B ..
-(r+1)*B - 1 of the same synthetic stream): weak scaling with no collective
-on the data path; a barrier brackets the timed region and rank 0 reports
-the max time over ranks.
+Under torchrun (N > 1) every rank verifies its own batch (rows starting at
+rank_row0(r) of the same seeded synthetic stream): weak scaling with no
+collective on the data path; a barrier brackets the timed region and rank 0
+reports the max time over ranks.
 """
 
 from __future__ import annotations
@@ -62,9 +62,17 @@ def parse():
                     help="c4 (token trees) is accepted in --ncu mode only")
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work of the oracle baseline (whole passes over the batch)")
     ap.add_argument("--ncu", action="store_true",
                     help="profiling mode: warm-up + steps calls of the workload, nothing else")
     return ap.parse_args()
+
+
+def rank_row0(rank: int) -> int:
+    """First row of rank `rank`'s batch in the seeded row stream (ranks never
+    share rows for batches below 100000 rows)."""
+    return rank * 100000
 
 
 def make_workload(name: str, row0: int = 0):
@@ -315,15 +323,18 @@ def other_workloads(sv, dev, stream, peak):
     return out
 
 
-def cpu_baseline(case, rows):
-    """The float64 oracle as it stands, single process, on `rows` batch rows."""
+def cpu_baseline(case, seconds):
+    """The float64 oracle as it stands, single process: whole passes over the
+    workload's batch rows, repeated until about `seconds` of CPU work."""
     import oracle
-    sub = case.select(rows)
-    args = sub.numpy64()
-    t = time.perf_counter()
-    oracle.verify_chain(*args)
-    dt = time.perf_counter() - t
-    return len(rows) * case.gamma / dt, dt
+    args = case.numpy64()
+    passes, dt = 0, 0.0
+    while dt < seconds or passes == 0:
+        t = time.perf_counter()
+        oracle.verify_chain(*args)
+        dt += time.perf_counter() - t
+        passes += 1
+    return passes * case.B * case.gamma / dt, dt, passes
 
 
 def dist_setup(n_gpus):
@@ -413,7 +424,7 @@ def main():
             sv.spec_verify_tree_greedy(*targs, tree.max_depth, stream=stream)
         torch.cuda.synchronize()
         return
-    case = make_workload(a.workload, row0=rank * 100000)
+    case = make_workload(a.workload, row0=rank_row0(rank))
     call = ChainCall(sv, case, dev, stream)
     call()
     torch.cuda.synchronize()
@@ -466,11 +477,10 @@ def main():
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1:
-        rows = list(range(min(case.B, 24)))
-        v, dt = cpu_baseline(case, rows)
+        v, dt, passes = cpu_baseline(case, a.cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"{len(rows)} of {case.B} batch rows of {case.name} "
-                                          f"({dt:.1f} s, single process)"}
+                                "sample": f"{passes} passes over the {case.B} batch rows of "
+                                          f"{case.name} ({dt:.1f} s, single process)"}
         if not a.quick:
             line["other_workloads"] = other_workloads(sv, dev, stream, peak)
     if rank == 0:
