@@ -26,10 +26,17 @@
  *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *  - `workspace` is caller-owned device memory of at least
  *    spec_verify_workspace_bytes(...) bytes, 16-byte aligned, with no
- *    initialisation required: every call first zeroes the workspace's small
- *    control block (one cudaMemsetAsync on `stream`).  Calls that may overlap
- *    on the GPU need distinct workspaces; calls in stream order may share one,
- *    whatever their shapes.
+ *    initialisation required.  Its first 4096 bytes hold library state
+ *    between calls (work-claim counters, left zeroed by every call and
+ *    stamped valid; a call that finds no valid stamp resets them itself).
+ *    A caller that writes into those 4096 bytes between calls must zero
+ *    them before the next call.  Calls that may overlap on the GPU need
+ *    distinct workspaces; calls in stream order may share one, whatever
+ *    their shapes.
+ *  - Each call enqueues its kernels as programmatic dependents
+ *    (programmatic dependent launch) of the work before them in `stream`:
+ *    the first kernel waits on the device for that work to complete before
+ *    it touches the workspace, so stream order is kept.
  *  - Row alignment is the caller's job: target row i scores draft i (the
  *    distribution conditioned on the context and drafts 0..i-1); row gamma is
  *    the bonus row.

@@ -20,7 +20,7 @@ int sm_count(int device) {
 }
 
 size_t workspace_bytes_any(int B, int rows, int V) {
-  const size_t a = make_layout(B, rows, V).total;
+  const size_t a = kPassHeaderBytes + make_layout(B, rows, V).total;
   // fp32 rows give the most warp-chunks
   const size_t b = make_pass_layout(B, rows, V, 4, 4, true).total;
   return a > b ? a : b;
@@ -51,7 +51,8 @@ static bool units_fit(long long B, long long per_batch) {
 }
 
 static void fill_workspace(KParams &P, void *ws, const Layout &L) {
-  char *w = static_cast<char *>(ws);
+  P.ws = static_cast<char *>(ws);
+  char *w = static_cast<char *>(ws) + kPassHeaderBytes;
   P.hdr = reinterpret_cast<WsHeader *>(w);
   P.a_count = reinterpret_cast<unsigned *>(w + L.a_count);
   P.b_count = reinterpret_cast<unsigned *>(w + L.b_count);

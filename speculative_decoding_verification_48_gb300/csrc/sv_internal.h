@@ -43,6 +43,11 @@ struct WsHeader {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// The first kPassHeaderBytes of every workspace hold the two-launch path's
+// state between calls (claim counters and their validity stamp); the
+// register-tile kernels' layout starts after them and never touches them.
+constexpr size_t kPassHeaderBytes = 4096;
+
 // Workspace layout for B batch rows of `rows` logit rows of V entries.  The
 // control block [0, ctrl) holds the work counters, per-row arrival counters,
 // decision flags and error words; every call zeroes it first (one small
@@ -92,6 +97,7 @@ struct KParams {
   int use_stream;             // allow the streaming (TMA ring) kernel
   int32_t *out_tokens, *out_nacc, *out_status, *out_path;
   float *out_diag;
+  char *ws;                   // workspace base
   WsHeader *hdr;
   unsigned *a_count, *b_count, *flag;
   int *err;                   // per-row SV_ROW_TIMEOUT bits from Phase-B waits

@@ -72,7 +72,7 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   }
   const int sms = sm_count(dev);
   if (sms <= 0) return SV_ERR_CUDA;
-  char *w = reinterpret_cast<char *>(P0.hdr);
+  char *w = P0.ws;
   PassParams S{};
   S.target = P0.target;
   S.draft = P0.draft;
@@ -114,6 +114,13 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   S.out_path = P0.out_path;
   S.out_diag = P0.out_diag;
   S.claim = reinterpret_cast<unsigned *>(w + L.claim);
+  S.claim_err = reinterpret_cast<unsigned long long *>(w + L.err);
+  S.claim_ready = reinterpret_cast<unsigned long long *>(w + L.ready);
+  S.claim_stamp = reinterpret_cast<unsigned long long *>(w + L.stamp);
+  {
+    static std::atomic<unsigned long long> calls{0};
+    S.call_id = calls.fetch_add(1, std::memory_order_relaxed) + 1;  // never 0
+  }
   S.done = reinterpret_cast<unsigned *>(w + L.done);
   S.part = reinterpret_cast<float2 *>(w + L.part);
   S.resid = reinterpret_cast<float *>(w + L.resid);
@@ -121,20 +128,35 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   const long long cap = (long long)sms * occ;
   int grid = (int)(want < cap ? want : cap);
   if (grid < 1) grid = 1;
-  if (cudaMemsetAsync(w, 0, L.ctrl, stream) != cudaSuccess) return SV_ERR_CUDA;
-  stats<<<grid, kPassThreads, 0, stream>>>(S);
-  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  // Both kernels are programmatic dependents of the work before them: the
+  // stats kernel of whatever the stream ran last (it waits on the device
+  // before touching the workspace), the decide kernel of the stats kernel.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  {
+    cudaLaunchConfig_t cs{};
+    cs.gridDim = dim3((unsigned)grid);
+    cs.blockDim = dim3(kPassThreads);
+    cs.dynamicSmemBytes = 0;
+    cs.stream = stream;
+    cs.attrs = attr;
+    cs.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cs, stats, S) != cudaSuccess) return SV_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(P0.B * H));
   cfg.blockDim = dim3(kPassThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decide, S) != cudaSuccess) return SV_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, decide, S) != cudaSuccess) {
+    // the claim counters were used and will not be reset: drop their stamp
+    // so the next call on this workspace resets them itself
+    (void)cudaMemsetAsync(S.claim_stamp, 0, sizeof(unsigned long long), stream);
+    return SV_ERR_CUDA;
+  }
   return SV_OK;
 }
 

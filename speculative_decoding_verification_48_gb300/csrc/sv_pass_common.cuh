@@ -27,6 +27,8 @@ constexpr int kResidBytes = 2048;  // one residual chunk of a row pair
 constexpr int kClaimStripes = 16;  // stats-kernel claim counters
 constexpr int kClaimStride = 32;   // 128 bytes between counters
 constexpr int kClaimProbes = 4096; // bound of the end-of-work probe loop
+constexpr long long kReadySpins = 4000000;  // bound of the counter-reset wait (about a second)
+constexpr unsigned long long kStampValid = 0x5356434c41494d30ull;
 
 template <int DT> struct Chunk {
   static constexpr int kEs = (int)sizeof(typename Elt<DT>::T);
@@ -80,17 +82,24 @@ struct PassParams {
   FastDiv fd_cT, fd_cP, fd_blk, fd_N;  // divisors of the unit decode: cT, cT + cD, B (cT + cD), N
   int32_t *out_tokens, *out_nacc, *out_status, *out_path;
   float *out_diag;
-  unsigned *claim;   // [kClaimStripes * kClaimStride] stats-kernel claim counters, then an
-                     // error word (nonzero: the claim probe bound was hit)
+  unsigned *claim;   // [kClaimStripes * kClaimStride] stats-kernel claim counters
+  unsigned long long *claim_err;    // == call_id: this call's stats kernel hit a bound
+  unsigned long long *claim_ready;  // == call_id: this call's stats kernel zeroed the counters
+  unsigned long long *claim_stamp;  // == kStampValid: the counters are zero (left so by the
+                                    // previous call's decide kernel)
+  unsigned long long call_id;       // unique per call, never 0
   unsigned *done;    // [B] residual-sweep arrivals
   float2 *part;      // [B][rows][cMax] warp-chunk partials
   float *resid;      // [B][cR] residual mass per chunk of the rejected row pair
 };
 
-// Workspace: claim counters, done[B] (together the control block [0, ctrl),
-// zeroed by every call), partials, residual chunk sums.
+// Workspace: a header of kPassHeaderBytes (claim counters, error, ready and
+// stamp words), done[B], partials, residual chunk sums.  No initialisation
+// is needed: each call's decide kernel leaves the counters zeroed and
+// stamps them valid, and a stats kernel that finds no valid stamp (a fresh
+// or overwritten workspace) zeroes them itself before any claim.
 struct PassLayout {
-  size_t claim, done, ctrl, part, resid, total;
+  size_t claim, err, ready, stamp, done, part, resid, total;
   int cT, cD, cMax, cR;
 };
 
@@ -102,10 +111,12 @@ inline PassLayout make_pass_layout(int B, int rows, int V, int esT, int esD, boo
   L.cD = stream_draft ? ceil_div(V, kChunkBytes / esD) : 0;
   L.cMax = L.cT > L.cD ? L.cT : L.cD;
   L.cR = ceil_div(V, kResidBytes / (esT > esD ? esT : esD));
-  size_t off = 0;
-  L.claim = off; off += (size_t)(kClaimStripes + 1) * kClaimStride * 4;
+  L.claim = 0;
+  L.err = (size_t)kClaimStripes * kClaimStride * 4;
+  L.ready = L.err + 128;
+  L.stamp = L.ready + 128;
+  size_t off = kPassHeaderBytes;
   L.done = off;  off = align_up(off + (size_t)B * 4, 256);
-  L.ctrl = off;
   L.part = off;  off = align_up(off + (size_t)B * rows * L.cMax * sizeof(float2), 256);
   L.resid = off; off = align_up(off + (size_t)B * L.cR * sizeof(float), 256);
   L.total = off;
@@ -118,6 +129,15 @@ inline PassLayout make_pass_layout(int B, int rows, int V, int esT, int esD, boo
 
 __device__ __forceinline__ unsigned ld_volatile_u32(const unsigned *p) {
   return *reinterpret_cast<const volatile unsigned *>(p);
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // 16-byte streaming load through the non-coherent path, no L1 allocation.

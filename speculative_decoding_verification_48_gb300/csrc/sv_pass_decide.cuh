@@ -79,8 +79,8 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     }
   }
   grid_dependency_wait();
-  unsigned claim_err = 0;
-  if (warp == 0) claim_err = __ldcg(P.claim + kClaimStripes * kClaimStride);
+  bool claim_err = false;
+  if (warp == 0) claim_err = __ldcg(P.claim_err) == P.call_id;
   if (badT) {
     if (warp == 0) {
       pass_error_row(P, b, SV_ROW_BAD_TEMPERATURE, G1, ot, nullptr);
@@ -292,7 +292,7 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
     if (n == 0 ? par != -1 : (par < 0 || par >= n)) flags |= SV_ROW_BAD_TREE;
     if (n > 0 && (tok < 0 || tok >= V)) flags |= SV_ROW_BAD_TOKEN;
   }
-  if (threadIdx.x == 0 && __ldcg(P.claim + kClaimStripes * kClaimStride)) flags |= SV_ROW_TIMEOUT;
+  if (threadIdx.x == 0 && __ldcg(P.claim_err) == P.call_id) flags |= SV_ROW_TIMEOUT;
   if (flags) atomicOr(&sm.flags, flags);
   __syncthreads();
   if (warp != 0) return;
@@ -332,10 +332,18 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
 
 template <int MODE, int TDT, int DDT, bool PROBS>
 __global__ void __launch_bounds__(kPassThreads, 4) sv_decide_kernel(const PassParams P) {
-  grid_dependency_wait();  // the stats kernel's partials and counters are complete
   const int b = blockIdx.x / P.H, h = blockIdx.x - b * P.H;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // the stats kernel has finished with its claim counters: leave them
+    // zeroed and stamped valid for the next call on this workspace
+    grid_dependency_wait();
+    for (int s = 0; s < kClaimStripes; ++s) P.claim[s * kClaimStride] = 0u;
+    __threadfence();
+    st_release_u64(P.claim_stamp, kStampValid);
+  }
   if (MODE == MODE_TREE) {
     __shared__ TreeSmem sm;
+    grid_dependency_wait();  // the stats kernel's partials are complete
     decide_tree<TDT>(P, b, sm);
   } else {
     __shared__ DecideSmem sm;

@@ -224,6 +224,29 @@ struct Claimer {
   int s;
 };
 
+__device__ __forceinline__ void claim_fail(const PassParams &P) {
+  if (lane_id() == 0) *reinterpret_cast<volatile unsigned long long *>(P.claim_err) = P.call_id;
+}
+
+// Bounded wait until this call's stats kernel has zeroed the counters (slow
+// path only); false, with the call flagged, if the bound is hit.
+__device__ __forceinline__ bool counters_reset_wait(const PassParams &P) {
+  bool ok = true;
+  if (lane_id() == 0) {
+    ok = false;
+    for (long long it = 0; it < kReadySpins; ++it) {
+      if (ld_acquire_u64(P.claim_ready) == P.call_id) {
+        ok = true;
+        break;
+      }
+      __nanosleep(32);
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) claim_fail(P);
+  return ok;
+}
+
 __device__ __forceinline__ unsigned claim_issue(const PassParams &P, const Claimer &c) {
   unsigned v = 0;
   if (lane_id() == 0) v = atomicAdd(P.claim + c.s * kClaimStride, 1u);
@@ -238,7 +261,7 @@ __device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, un
   // practice — if it were, the call is flagged rather than left unfinished
   for (int probe = 0; k >= P.total; ++probe) {
     if (probe == kClaimProbes) {
-      if (lane == 0) atomicOr(P.claim + kClaimStripes * kClaimStride, 1u);
+      claim_fail(P);
       return -1;
     }
     unsigned cnt = 0xffffffffu;
@@ -257,7 +280,26 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
   // The decide kernel may launch at once: its CTAs take the place of
   // finished stats CTAs and wait on the device for this grid to complete.
   grid_dependents_launch();
+  // This kernel is itself a programmatic dependent of whatever the stream
+  // ran before (typically the previous call's decide kernel): nothing of the
+  // workspace is touched before that work has completed.
+  grid_dependency_wait();
+  // residual-sweep arrival counters of this call start at zero (the decide
+  // kernel reads them only after this grid has completed)
+  for (int i = blockIdx.x * kPassThreads + threadIdx.x; i < P.B; i += gridDim.x * kPassThreads)
+    P.done[i] = 0u;
+  // Claim counters: zero and stamped valid by the previous call's decide
+  // kernel, else (fresh or overwritten workspace) zeroed here by thread 0 of
+  // CTA 0 while every warp waits.  The stamp is not written while this grid
+  // runs, so all warps take the same path.
+  const bool stamped = ld_acquire_u64(P.claim_stamp) == kStampValid;
+  if (!stamped && blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int s = 0; s < kClaimStripes; ++s) P.claim[s * kClaimStride] = 0u;
+    __threadfence();
+    st_release_u64(P.claim_ready, P.call_id);
+  }
   Claimer cl{(int)((blockIdx.x * kPassWarps + warp_id()) % kClaimStripes)};
+  if (!stamped && !counters_reset_wait(P)) return;
   uint4 b0[kChunkVecs], b1[kChunkVecs];
   int ka = claim_resolve(P, cl, claim_issue(P, cl));
   if (ka >= 0) {
