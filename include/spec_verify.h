@@ -212,8 +212,8 @@ SV_API const char *spec_verify_status_string(sv_status s);
  *  - Every call on a device shares the one array.  Calls that may overlap
  *    on the GPU (different streams, or different host threads without
  *    ordering) race on it and give wrong results: keep them in one stream
- *    order.  Each call zeroes the array's control block before its kernel
- *    runs, so what an earlier call left there does no harm.
+ *    order.  What an earlier call left in the array does no harm: every
+ *    call either finds its state valid or resets it.
  */
 SV_API sv_status spec_verify_chain_no_alloc(const void *target_logits, sv_dtype tdt,
                                             const void *draft, sv_dtype ddt, int draft_is_probs,

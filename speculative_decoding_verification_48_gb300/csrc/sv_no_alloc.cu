@@ -59,9 +59,9 @@ SV_API sv_status spec_verify_chain_no_alloc(const void *target_logits, sv_dtype 
   if (need > (size_t)SV_NO_ALLOC_SCRATCH_BYTES) return SV_ERR_UNSUPPORTED;
   void *scratch = scratch_on_current_device();
   if (scratch == nullptr) return SV_ERR_CUDA;
-  // The regular entry point zeroes the control block of its workspace at the
-  // start of every call, so what the previous call left in the array does
-  // not matter.
+  // The regular entry point needs no initialised workspace (every call either
+  // finds the state that the previous call left valid or resets it), so what
+  // an earlier call left in the array does not matter.
   return spec_verify_chain(target_logits, tdt, draft, ddt, draft_is_probs, draft_tokens,
                            temperatures, uniforms, B, gamma, V, out_tokens, out_num_accepted,
                            out_diag, out_row_status, scratch,
