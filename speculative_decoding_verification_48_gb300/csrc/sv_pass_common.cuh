@@ -194,6 +194,49 @@ __device__ __forceinline__ float resid_term(float lp, float lq, const ResidCoef 
   return max_nan(0.f, p - q);
 }
 
+// Packed pairs of fp32 (sm_100+ two-wide FMA / ADD): one instruction for
+// two lanes of work.
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// resid_term for two neighbouring elements through the two-wide FMA: the
+// same values as two resid_term calls (fma.rn per lane, p - q rounded once).
+template <bool PROBS>
+__device__ __forceinline__ float2 resid_pair(float lp0, float lp1, float lq0, float lq1,
+                                             const ResidCoef &k) {
+  const unsigned long long c2 = f2_pack(k.c, k.c);
+  const float2 pe = f2_unpack(f2_fma(f2_pack(lp0, lp1), c2, f2_pack(k.ap, k.ap)));
+  const unsigned long long p2 = f2_pack(ex2(pe.x), ex2(pe.y));
+  unsigned long long q2;
+  if (PROBS) {
+    q2 = f2_pack(lq0, lq1);
+  } else {
+    const float2 qe = f2_unpack(f2_fma(f2_pack(lq0, lq1), c2, f2_pack(k.aq, k.aq)));
+    q2 = f2_pack(ex2(qe.x), ex2(qe.y));
+  }
+  const float2 d = f2_unpack(f2_fma(q2, f2_pack(-1.f, -1.f), p2));  // p - q
+  return make_float2(max_nan(0.f, d.x), max_nan(0.f, d.y));
+}
+
 // Wait for the grid this one depends on (programmatic dependent launch);
 // returns at once when the launch had no such dependency.
 __device__ __forceinline__ void grid_dependency_wait() {

@@ -68,6 +68,8 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   int x = 0;
   bool tok_ok = false;
   float lp = 0.f, lq = 0.f, qp = 0.f, ui = 0.f;
+  // the categorical draw, used by warp 0 of whichever CTA draws the token
+  const float ug = (warp == 0 && !badT && !greedy) ? __ldg(P.unif + (size_t)b * G1 + g) : 0.f;
   if (act) {
     x = __ldg(P.draft_tokens + (size_t)b * g + i);
     tok_ok = x >= 0 && x < V;
@@ -178,10 +180,10 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     } else {
       const float2 *pr = pb + (size_t)g * P.cMax;
       tok_j = warp_sample_softmax_row<TDT>(tgt + (size_t)g * V, pr, P.cT, V, sm.rowM[g], c,
-                                           __ldg(P.unif + (size_t)b * G1 + g));
+                                           ug);
     }
     for (int s = lane; s < G1; s += 32)
-      ot[s] = s < j ? __ldg(P.draft_tokens + (size_t)b * g + s) : (s == j ? tok_j : -1);
+      ot[s] = s < j ? x : (s == j ? tok_j : -1);  // lane s holds draft token s
     if (lane == 0) {
       P.out_nacc[b] = j;
       if (P.out_status) P.out_status[b] = 0;
@@ -214,7 +216,7 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
         rq[u].load(qrow + x0 + e);
       }
     }
-    float s = 0.f;
+    unsigned long long s2 = 0ull;  // (+0, +0)
 #pragma unroll
     for (int u = 0; u < PC::kVecs; ++u) {
       const int e = (lane + 32 * u) * PC::kVec;
@@ -223,10 +225,14 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
         ra[u].unpack(a);
         rq[u].unpack(q);
 #pragma unroll
-        for (int t = 0; t < PC::kVec; ++t) s += resid_term<PROBS>(a[t], q[t], rk);
+        for (int t = 0; t < PC::kVec; t += 2) {
+          const float2 r = resid_pair<PROBS>(a[t], a[t + 1], q[t], q[t + 1], rk);
+          s2 = f2_add(s2, f2_pack(r.x, r.y));
+        }
       }
     }
-    s = warp_sum(s);
+    const float2 sp = f2_unpack(s2);
+    float s = warp_sum(sp.x + sp.y);
     if (lane == 0) rs[ch] = s;
   }
   __syncthreads();
@@ -239,7 +245,7 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   __syncthreads();
   if (!sm.last || warp != 0) return;
   // 5. the last CTA: crossing chunk of u * R, then a rescan of that chunk
-  const float u = __ldg(P.unif + (size_t)b * G1 + g);
+  const float u = ug;
   float R = 0.f, base = 0.f;
   const int t = warp_chunk_cross(P.cR, [&](int k) { return __ldcg(rs + k); }, u, R, base);
   if (isnan(R) || isinf(R)) {
@@ -262,7 +268,7 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     k = x0 + warp_rescan<PC::kPer>(a, base, target);
   }
   for (int s = lane; s < G1; s += 32)
-    ot[s] = s < j ? __ldg(P.draft_tokens + (size_t)b * g + s) : (s == j ? k : -1);
+    ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
   if (lane == 0) {
     P.out_nacc[b] = j;
     if (P.out_status) P.out_status[b] = 0;

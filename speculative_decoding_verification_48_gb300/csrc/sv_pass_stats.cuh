@@ -171,13 +171,21 @@ __device__ __forceinline__ void chunk_reduce(const ChunkRef &r, const uint4 (&bu
       const float mc = m * c;
       if (fabsf(mc) <= 1.0e37f) {
         const float d = fmaf(m, c, -mc);
+        // element pairs through the two-wide FMA and ADD
+        const unsigned long long c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
+        unsigned long long acc[2] = {0ull, 0ull};  // (+0, +0) pairs
 #pragma unroll
         for (int u = 0; u < kChunkVecs; ++u) {
           float v[VEC];
           Elt<DT>::unpack(buf[u], v);
 #pragma unroll
-          for (int t = 0; t < VEC; ++t) s4[t & 3] += ex2(fmaf(v[t], c, -mc));
+          for (int t = 0; t < VEC; t += 2) {
+            const float2 e = f2_unpack(f2_fma(f2_pack(v[t], v[t + 1]), c2, nmc2));
+            acc[(t >> 1) & 1] = f2_add(acc[(t >> 1) & 1], f2_pack(ex2(e.x), ex2(e.y)));
+          }
         }
+        const float2 a0 = f2_unpack(acc[0]), a1 = f2_unpack(acc[1]);
+        s4[0] = a0.x; s4[1] = a0.y; s4[2] = a1.x; s4[3] = a1.y;
         scale = ex2(-d);
       } else {
 #pragma unroll
