@@ -298,6 +298,38 @@ def other_workloads(sv, dev, stream, peak):
         out[case.name] = {"us_per_call": ms * 1e3, "positions_per_s": case.B * case.gamma / (ms * 1e-3),
                           "GBps": nbytes / (ms * 1e-3) / 1e9, "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
                           "algorithmic_bytes": nbytes, "l2": "flushed before each call (256 MB read)"}
+    # C1 and C2 as batches of independent rounds in one call each (the
+    # throughput a batched decode loop sees); C1's batch fits in L2 and is
+    # flushed before each call, C2's 1024-round batch (720 MB) is not
+    for label, case, steps, flush_each in (
+            ("c1_batched_256_rounds", W.c1_chain_fp32_v1000(rounds=256), 200, True),
+            ("c2_batched_1024_rounds_T1.0", W.c2_chain_bf16_v32000(1.0, rounds=1024), 50, False)):
+        call = ChainCall(sv, case, dev, stream)
+        call()
+        torch.cuda.synchronize()
+        nbytes = W.chain_algorithmic_bytes(case, call.out[1].cpu().numpy())
+        if flush_each:
+            times = []
+            for i in range(steps):
+                with torch.cuda.stream(stream):
+                    flush.sum()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                call()
+                b.record(stream)
+                b.synchronize()
+                times.append(a.elapsed_time(b))
+            ms = float(np.median(times))
+        else:
+            total, ms, _ = time_calls(call, steps, 5, stream, per_call_events=False)
+        out[label] = {"us_per_call": ms * 1e3, "positions_per_s": case.B * case.gamma / (ms * 1e-3),
+                      "GBps": nbytes / (ms * 1e-3) / 1e9,
+                      "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
+                      "algorithmic_bytes": nbytes,
+                      "l2": "flushed before each call (256 MB read)" if flush_each
+                            else "inputs larger than L2, back-to-back calls"}
+        del call
     tree = W.c4_tree_f16_v32000()
     args = [t.to(dev) for t in (tree.node_logits, tree.parent, tree.node_tokens)]
     res = sv.spec_verify_tree_greedy(*args, tree.max_depth, stream=stream)

@@ -356,3 +356,57 @@ def verify_tree_greedy(node_logits, parent, node_tokens, max_depth):
         tokens[b, d] = a[cur]
         n_acc[b] = d
     return dict(path=path, tokens=tokens, num_accepted=n_acc, status=status)
+
+
+# --------------------------------------------------------------------------
+# Draft-side sampling (the draft step that produces x_i ~ q)
+# --------------------------------------------------------------------------
+
+def draft_sample(logits, temperatures, uniforms):
+    """One categorical draw per row from the draft distribution.
+
+    [SpS] §アルゴリズム Step 1 and the ``speculative_decode`` listing: the
+    draft model's next-token row goes through softmax(logits / T) and one
+    token is drawn from it (``torch.multinomial``).  Readings shared with
+    verification: the draw is the inverse CDF in ascending vocabulary order
+    with the row's uniform (``inverse_cdf``); T <= 0 takes the first argmax.
+
+    Inputs: logits [B, V], temperatures [B], uniforms [B] in [0, 1).
+    Returns dict(tokens [B] int64, probs [B] float64 = q(token) (0 for greedy
+    rows), status [B], cdf_lo [B], cdf_hi [B] = C(k-1)/R and C(k)/R of the
+    drawn token (NaN for greedy or failed rows), for boundary accounting).
+    Status: a NaN / +inf / all -inf softmax row or a NaN argmax row flags
+    ROW_NONFINITE; a NaN temperature or one in (0, 1e-20) flags
+    ROW_BAD_TEMPERATURE; such rows get token -1.
+    """
+    l = np.asarray(logits, np.float64)
+    T = np.asarray(temperatures, np.float64)
+    u = np.asarray(uniforms, np.float64)
+    B, V = l.shape
+    tokens = np.full(B, -1, np.int64)
+    probs = np.zeros(B)
+    status = np.zeros(B, np.int64)
+    lo = np.full(B, np.nan)
+    hi = np.full(B, np.nan)
+    for b in range(B):
+        t = T[b]
+        if np.isnan(t) or (0.0 < t < TINY_T):
+            status[b] = ROW_BAD_TEMPERATURE
+            continue
+        if t <= 0:
+            if np.isnan(l[b]).any():
+                status[b] = ROW_NONFINITE
+                continue
+            tokens[b] = int(first_argmax(l[b]))
+            continue
+        p = tempered_softmax(l[b][None], np.array([t]))[0]
+        if not np.all(np.isfinite(p)):
+            status[b] = ROW_NONFINITE
+            continue
+        k, C, R = inverse_cdf(p[None], np.array([u[b]]))
+        k = int(k[0])
+        tokens[b] = k
+        probs[b] = p[k]
+        lo[b] = (C[0, k - 1] if k > 0 else 0.0) / R[0]
+        hi[b] = C[0, k] / R[0]
+    return dict(tokens=tokens, probs=probs, status=status, cdf_lo=lo, cdf_hi=hi)
