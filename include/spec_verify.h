@@ -99,7 +99,8 @@ typedef struct CUstream_st *sv_stream_t;
  * `rows_per_batch` logit rows of V elements each.  rows_per_batch is
  * 2*gamma+1 for spec_verify_chain with draft logits, gamma+1 for
  * spec_verify_chain with draft probabilities and for
- * spec_verify_chain_greedy, and N for spec_verify_tree_greedy.  `dt` is the
+ * spec_verify_chain_greedy, N for spec_verify_tree_greedy, and 1 for
+ * spec_draft_sample.  `dt` is the
  * logit dtype.  Returns 0 for non-positive sizes.
  */
 SV_API size_t spec_verify_workspace_bytes(int B, int rows_per_batch, int V, sv_dtype dt);
@@ -180,6 +181,27 @@ SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
                                          int32_t *out_num_accepted, int32_t *out_row_status,
                                          void *workspace, size_t workspace_bytes,
                                          sv_stream_t stream);
+
+/*
+ * Draft-side categorical draw, one per row: the draft step that produces
+ * the tokens verified above ("論文解説: Speculative Sampling", §アルゴリズム
+ * Step 1: each draft token is drawn from softmax(draft logits / T)).
+ *  logits       [B, V] of dtype dt (the draft model's next-token rows).
+ *  temperatures fp32 [B]; T <= 0 takes the first argmax (lowest index).
+ *  uniforms     fp32 [B] in [0, 1): the draw is the inverse CDF in
+ *               ascending vocabulary order, the smallest k with
+ *               sum_{x<=k} q(x) > u * sum_x q(x), q = softmax(logits / T).
+ *  out_tokens   int32 [B]: the drawn token (-1 for an invalid row).
+ *  out_probs    nullable fp32 [B]: q(token) (0 for greedy and invalid rows).
+ *  out_row_status nullable int32 [B]: SV_ROW_* bits.
+ *  workspace: spec_verify_workspace_bytes(B, 1, V, dt) bytes.
+ *  Rows must start on 16-byte boundaries (16-byte aligned `logits`, V times
+ *  the element size a multiple of 16); otherwise SV_ERR_UNSUPPORTED.
+ */
+SV_API sv_status spec_draft_sample(const void *logits, sv_dtype dt, const float *temperatures,
+                                   const float *uniforms, int B, int V, int32_t *out_tokens,
+                                   float *out_probs, int32_t *out_row_status, void *workspace,
+                                   size_t workspace_bytes, sv_stream_t stream);
 
 /* Static description of a status code; never NULL. */
 SV_API const char *spec_verify_status_string(sv_status s);

@@ -75,6 +75,9 @@ def lib() -> ctypes.CDLL:
                                                   _INT, _I32P, _I32P, _I32P, _I32P, _VP,
                                                   _SIZE, _VP]
             L.spec_verify_tree_greedy.restype = _INT
+            L.spec_draft_sample.argtypes = [_VP, _INT, _F32P, _F32P, _INT, _INT, _I32P, _F32P,
+                                             _I32P, _VP, _SIZE, _VP]
+            L.spec_draft_sample.restype = _INT
             L.spec_verify_status_string.argtypes = [_INT]
             L.spec_verify_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -251,3 +254,37 @@ def spec_verify_tree_greedy(node_logits: torch.Tensor, parent: torch.Tensor,
     if st != 0:
         raise SpecVerifyError(st, "spec_verify_tree_greedy")
     return out_path, out_tokens, out_num_accepted, out_row_status
+
+
+def spec_draft_sample(logits: torch.Tensor, temperatures: torch.Tensor, uniforms: torch.Tensor,
+                      out_tokens=None, out_probs=None, out_row_status=None, workspace=None,
+                      stream=None):
+    """Draft-side categorical draw per row (see spec_draft_sample in spec_verify.h).
+
+    logits [B, V] (fp32 / bf16 / fp16, rows 16-byte aligned), temperatures
+    fp32 [B], uniforms fp32 [B].  Returns (tokens int32 [B], probs fp32 [B],
+    row_status int32 [B])."""
+    dev = logits.device
+    B, V = logits.shape
+    _check(logits, "logits", device=dev)
+    if logits.dtype not in _DT:
+        raise TypeError("logits dtype must be float32, bfloat16 or float16")
+    _check(temperatures, "temperatures", torch.float32, (B,), dev)
+    _check(uniforms, "uniforms", torch.float32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_probs is None:
+        out_probs = torch.empty((B,), dtype=torch.float32, device=dev)
+    if out_row_status is None:
+        out_row_status = torch.empty((B,), dtype=torch.int32, device=dev)
+    sp = _stream_ptr(dev, stream)
+    nbytes = spec_verify_workspace_bytes(B, 1, V, _DT[logits.dtype])
+    if workspace is None:
+        workspace = workspace_for(dev, sp, nbytes)
+    st = lib().spec_draft_sample(logits.data_ptr(), _DT[logits.dtype], temperatures.data_ptr(),
+                                 uniforms.data_ptr(), B, V, out_tokens.data_ptr(),
+                                 out_probs.data_ptr(), out_row_status.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(), sp)
+    if st != 0:
+        raise SpecVerifyError(st, "spec_draft_sample")
+    return out_tokens, out_probs, out_row_status

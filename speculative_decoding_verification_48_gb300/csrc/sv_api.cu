@@ -209,6 +209,39 @@ SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
   return launch_tree(P, dt, reinterpret_cast<cudaStream_t>(stream));
 }
 
+SV_API sv_status spec_draft_sample(const void *logits, sv_dtype dt, const float *temperatures,
+                                   const float *uniforms, int B, int V, int32_t *out_tokens,
+                                   float *out_probs, int32_t *out_row_status, void *workspace,
+                                   size_t workspace_bytes, sv_stream_t stream) {
+  if (!logits || !temperatures || !uniforms || !out_tokens || !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (B < 1 || V < 1 || V > SV_MAX_VOCAB) return SV_ERR_INVALID_ARG;
+  if (!valid_dtype(dt)) return SV_ERR_INVALID_ARG;
+  if (!aligned_to(temperatures, 4) || !aligned_to(uniforms, 4) || !aligned_to(out_tokens, 4) ||
+      !aligned_to(out_probs, 4) || !aligned_to(out_row_status, 4))
+    return SV_ERR_INVALID_ARG;
+  // rows must start on 16-byte boundaries (the streaming path only)
+  if ((reinterpret_cast<uintptr_t>(logits) & 15) || ((size_t)V * dtype_size(dt)) % 16)
+    return SV_ERR_UNSUPPORTED;
+  if (workspace_bytes < workspace_bytes_any(B, 1, V) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 15))
+    return SV_ERR_INVALID_ARG;
+  KParams P{};
+  P.target = logits;
+  P.temps = temperatures;
+  P.unif = uniforms;
+  P.B = B;
+  P.N = 1;
+  P.V = V;
+  P.rows = 1;
+  P.use_stream = 1;
+  P.out_tokens = out_tokens;
+  P.out_diag = out_probs;
+  P.out_status = out_row_status;
+  fill_workspace(P, workspace, make_layout(B, 1, V));
+  return launch_draft(P, dt, reinterpret_cast<cudaStream_t>(stream));
+}
+
 SV_API const char *spec_verify_status_string(sv_status s) {
   switch (s) {
     case SV_OK: return "SV_OK: success";

@@ -21,4 +21,24 @@ sv_status launch_tree(const KParams &P, sv_dtype dt, cudaStream_t stream) {
   return SV_ERR_UNSUPPORTED;
 }
 
+// Draft-side draws: the two-launch path only (rows start on 16-byte
+// boundaries, checked by the caller).
+template <int DT>
+static sv_status launch_draft_t(const KParams &P, cudaStream_t stream) {
+  constexpr int es = (DT == SV_F32) ? 4 : 2;
+  const PassLayout L = make_pass_layout(P.B, 1, P.V, es, es, false);
+  const long long total = pass_units<MODE_DRAFT, DT, DT, false>(P, L);
+  if (total < 0) return SV_ERR_UNSUPPORTED;
+  return launch_pass<MODE_DRAFT, DT, DT, false>(P, L, total, stream);
+}
+
+sv_status launch_draft(const KParams &P, sv_dtype dt, cudaStream_t stream) {
+  switch (dt) {
+    case SV_F32: return launch_draft_t<SV_F32>(P, stream);
+    case SV_BF16: return launch_draft_t<SV_BF16>(P, stream);
+    case SV_F16: return launch_draft_t<SV_F16>(P, stream);
+  }
+  return SV_ERR_UNSUPPORTED;
+}
+
 }  // namespace sv

@@ -20,7 +20,7 @@ constexpr int kTile = 8192;
 constexpr int kPer = kTile / kThreads;
 constexpr int kMaxRows = 2 * SV_MAX_GAMMA + 1;
 
-enum Mode { MODE_CHAIN = 0, MODE_CHAIN_GREEDY = 1, MODE_TREE = 2 };
+enum Mode { MODE_CHAIN = 0, MODE_CHAIN_GREEDY = 1, MODE_TREE = 2, MODE_DRAFT = 3 };
 enum DecKind { DEC_DONE = 0, DEC_RESIDUAL = 1 };
 
 // Per-batch-row decision written by the CTA that completes the row's
@@ -115,6 +115,7 @@ sv_status launch_chain_bf16(const KParams &P, sv_dtype ddt, bool probs, cudaStre
 sv_status launch_chain_f16(const KParams &P, sv_dtype ddt, bool probs, cudaStream_t stream);
 sv_status launch_chain_greedy(const KParams &P, sv_dtype tdt, cudaStream_t stream);
 sv_status launch_tree(const KParams &P, sv_dtype dt, cudaStream_t stream);
+sv_status launch_draft(const KParams &P, sv_dtype dt, cudaStream_t stream);
 
 // Device properties cached per device (host side).
 int sm_count(int device);

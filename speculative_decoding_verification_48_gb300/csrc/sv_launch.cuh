@@ -42,7 +42,7 @@ sv_status launch_phase(const KParams &P0, const Sched &s, cudaStream_t stream) {
 template <int MODE, int TDT, int DDT, bool PROBS>
 long long pass_units(const KParams &P, const PassLayout &L) {
   long long total;
-  if (MODE == MODE_TREE) total = (long long)P.B * P.N * L.cT;
+  if (MODE == MODE_TREE || MODE == MODE_DRAFT) total = (long long)P.B * P.N * L.cT;
   else total = (long long)P.B * L.cT + (long long)P.gamma * P.B * (L.cT + L.cD);
   return total < (1LL << 31) - 1 ? total : -1;
 }
@@ -145,7 +145,8 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
     if (cudaLaunchKernelEx(&cs, stats, S) != cudaSuccess) return SV_ERR_CUDA;
   }
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)(P0.B * H));
+  cfg.gridDim = dim3((unsigned)(MODE == MODE_DRAFT ? (P0.B + kPassWarps - 1) / kPassWarps
+                                                  : P0.B * H));  // a draft row per warp
   cfg.blockDim = dim3(kPassThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

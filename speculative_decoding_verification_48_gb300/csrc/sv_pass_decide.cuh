@@ -336,6 +336,43 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
   }
 }
 
+// Draft-side draw, one warp per row ("論文解説: Speculative Sampling",
+// §アルゴリズム Step 1: the draft token is drawn from softmax(draft logits / T);
+// the draw is the inverse CDF in vocabulary order with the row's uniform,
+// and T <= 0 takes the first argmax).  out_diag carries q(token).
+template <int DT>
+__device__ void decide_draft_row(const PassParams &P, int b) {
+  using TT = typename Elt<DT>::T;
+  const int lane = lane_id(), V = P.V;
+  const float T = __ldg(P.temps + b);
+  const TT *row = reinterpret_cast<const TT *>(P.target) + (size_t)b * V;
+  const float2 *pr = P.part + (size_t)b * P.cMax;
+  int status = 0, tok = -1;
+  float prob = 0.f;
+  if (bad_temperature(T)) {
+    status = SV_ROW_BAD_TEMPERATURE;
+  } else if (T <= 0.f) {
+    const float2 mi = warp_row_argmax(pr, P.cT);
+    if (isnan(mi.x)) status = SV_ROW_NONFINITE;
+    else tok = __float_as_int(mi.y);
+  } else {
+    const float c = kLog2e / T;
+    const float2 mz = warp_row_softmax(pr, P.cT, c);
+    if (!(mz.y > 0.f && mz.y <= 3.0e38f)) {
+      status = SV_ROW_NONFINITE;
+    } else {
+      tok = warp_sample_softmax_row<DT>(row, pr, P.cT, V, mz.x, c, __ldg(P.unif + b));
+      prob = ex2((Elt<DT>::load1(row + tok) - mz.x) * c) / mz.y;
+    }
+  }
+  if (__ldcg(P.claim_err) == P.call_id) status = SV_ROW_TIMEOUT;
+  if (lane == 0) {
+    P.out_tokens[b] = status ? -1 : tok;
+    if (P.out_diag) P.out_diag[b] = status ? 0.f : prob;
+    if (P.out_status) P.out_status[b] = status;
+  }
+}
+
 template <int MODE, int TDT, int DDT, bool PROBS>
 __global__ void __launch_bounds__(kPassThreads, 4) sv_decide_kernel(const PassParams P) {
   const int b = blockIdx.x / P.H, h = blockIdx.x - b * P.H;
@@ -346,6 +383,12 @@ __global__ void __launch_bounds__(kPassThreads, 4) sv_decide_kernel(const PassPa
     for (int s = 0; s < kClaimStripes; ++s) P.claim[s * kClaimStride] = 0u;
     __threadfence();
     st_release_u64(P.claim_stamp, kStampValid);
+  }
+  if (MODE == MODE_DRAFT) {
+    grid_dependency_wait();  // the stats kernel's partials are complete
+    const int r = blockIdx.x * kPassWarps + warp_id();  // one warp per row
+    if (r < P.B) decide_draft_row<TDT>(P, r);
+    return;
   }
   if (MODE == MODE_TREE) {
     __shared__ TreeSmem sm;

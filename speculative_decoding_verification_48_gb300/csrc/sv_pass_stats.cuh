@@ -37,8 +37,9 @@ template <int MODE, int TDT, int DDT, bool PROBS>
 __device__ __forceinline__ ChunkRef decode_chunk(const PassParams &P, int k) {
   ChunkRef r;
   int b, row, ci, draft = 0, pos = 0;
-  if (MODE == MODE_TREE) {
-    const int gr = (int)fdiv((unsigned)k, P.fd_cT);  // global node row b * N + n
+  if (MODE == MODE_TREE || MODE == MODE_DRAFT) {
+    // global row b * N + n (a draft batch has N = 1 row per batch entry)
+    const int gr = (int)fdiv((unsigned)k, P.fd_cT);
     ci = k - gr * P.cT;
     b = (int)fdiv((unsigned)gr, P.fd_N);
     row = gr - b * P.N;
@@ -68,7 +69,7 @@ __device__ __forceinline__ ChunkRef decode_chunk(const PassParams &P, int k) {
   r.draft = draft;
   r.dst = P.part + ((size_t)b * P.rows + row) * P.cMax + ci;
   r.c = 0.f;
-  if (MODE == MODE_CHAIN) {
+  if (MODE == MODE_CHAIN || MODE == MODE_DRAFT) {
     const float T = __ldg(P.temps + b);
     if (bad_temperature(T)) r.kind = CK_SKIP;
     else if (T > 0.f) { r.kind = CK_SOFTMAX; r.c = kLog2e / T; }
@@ -81,7 +82,7 @@ __device__ __forceinline__ ChunkRef decode_chunk(const PassParams &P, int k) {
     r.src = d + ((size_t)b * P.gamma + pos) * P.V + r.x0;
   } else {
     const auto *t = reinterpret_cast<const typename Elt<TDT>::T *>(P.target);
-    const int rows_per = (MODE == MODE_TREE) ? P.N : P.gamma + 1;
+    const int rows_per = (MODE == MODE_TREE || MODE == MODE_DRAFT) ? P.N : P.gamma + 1;
     r.src = t + ((size_t)b * rows_per + row) * P.V + r.x0;
   }
   return r;

@@ -307,3 +307,44 @@ def chain_algorithmic_bytes(case: ChainCase, num_accepted: Optional[np.ndarray] 
 def tree_algorithmic_bytes(case: TreeCase) -> int:
     B, N, V = case.B, case.N, case.V
     return int(B * N * V * case.node_logits.element_size() + 2 * B * N * 4)
+
+
+@dataclass
+class DraftCase:
+    """Draft-side draws: one logit row per batch entry."""
+    name: str
+    logits: torch.Tensor        # [B, V]
+    temperatures: torch.Tensor  # [B]
+    uniforms: torch.Tensor      # [B]
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def B(self): return self.logits.shape[0]
+
+    @property
+    def V(self): return self.logits.shape[1]
+
+    def numpy64(self):
+        return to_f64(self.logits), self.temperatures.double().numpy(), self.uniforms.double().numpy()
+
+
+def make_draft(name: str, seed: int, B: int, V: int, dtype: str = "bf16", target: str = "zipf",
+               sigma: float = 1.0, temperature: Callable[[int, float], float] | float = 1.0,
+               row0: int = 0) -> DraftCase:
+    """Draft-model next-token rows: N(0, sigma^2) (+ Zipf bias -1.1 ln(rank)),
+    a temperature per row (constant or (b, v) -> T of a per-row uniform v)
+    and one uniform per row; row b uses the generator (seed, row0 + b)."""
+    bias = zipf_bias(seed, V) if target == "zipf" else None
+    logits = torch.empty((B, V), dtype=DTYPES[dtype])
+    temps = torch.empty(B, dtype=torch.float32)
+    unif = torch.empty(B, dtype=torch.float32)
+    for i in range(B):
+        g = gen_for(seed, row0 + i)
+        row = torch.randn(V, generator=g) * float(sigma)
+        if bias is not None:
+            row += bias
+        v = uniform(g)
+        temps[i] = float(temperature(row0 + i, v)) if callable(temperature) else float(temperature)
+        unif[i] = torch.rand(1, generator=g)[0]
+        logits[i] = row.to(DTYPES[dtype])
+    return DraftCase(name, logits, temps, unif, dict(seed=seed, dtype=dtype))
