@@ -330,6 +330,26 @@ def other_workloads(sv, dev, stream, peak):
                       "l2": "flushed before each call (256 MB read)" if flush_each
                             else "inputs larger than L2, back-to-back calls"}
         del call
+    # draft-side draws (the draft step before verification): 1024 rows of
+    # the 128K vocabulary, back to back (262 MB > L2)
+    dcase = W.make_draft("draft_sample_B1024_V128256_bf16", 1006, 1024, 128256, "bf16",
+                         temperature=lambda b, v: 0.0 if b % 8 == 0 else 0.2 + v)
+    dl, dT, du = (t.to(dev) for t in (dcase.logits, dcase.temperatures, dcase.uniforms))
+    douts = sv.spec_draft_sample(dl, dT, du, stream=stream)
+    dws = torch.zeros(sv.spec_verify_workspace_bytes(dcase.B, 1, dcase.V, 1), dtype=torch.uint8,
+                      device=dev)
+
+    def dcall():
+        sv.spec_draft_sample(dl, dT, du, out_tokens=douts[0], out_probs=douts[1],
+                             out_row_status=douts[2], workspace=dws, stream=stream)
+    _, dms, _ = time_calls(dcall, 50, 5, stream, per_call_events=False)
+    dbytes = dcase.B * dcase.V * 2 + dcase.B * 8
+    out[dcase.name] = {"us_per_call": dms * 1e3, "rows_per_s": dcase.B / (dms * 1e-3),
+                       "GBps": dbytes / (dms * 1e-3) / 1e9,
+                       "frac_of_peak": dbytes / (dms * 1e-3) / 1e9 / peak,
+                       "algorithmic_bytes": dbytes,
+                       "l2": "inputs larger than L2, back-to-back calls"}
+    del dl, dT, du, douts, dws
     tree = W.c4_tree_f16_v32000()
     args = [t.to(dev) for t in (tree.node_logits, tree.parent, tree.node_tokens)]
     res = sv.spec_verify_tree_greedy(*args, tree.max_depth, stream=stream)
