@@ -410,3 +410,41 @@ def draft_sample(logits, temperatures, uniforms):
         lo[b] = (C[0, k - 1] if k > 0 else 0.0) / R[0]
         hi[b] = C[0, k] / R[0]
     return dict(tokens=tokens, probs=probs, status=status, cdf_lo=lo, cdf_hi=hi)
+
+
+# --------------------------------------------------------------------------
+# Token-tree attention mask
+# --------------------------------------------------------------------------
+
+def tree_ancestor_mask(parent):
+    """Ancestor mask of every node of every token tree.
+
+    [SpecInfer] §技術の仕組み › 基本アイデア and §推論方法: all tree nodes are
+    scored in one target pass, which needs a topology-aware attention mask —
+    a node sees itself and its ancestors (the path from the root), not its
+    siblings or their subtrees.  Reading: mask[b, n, m] is True iff m == n
+    or m is an ancestor of n; depth[b, n] counts the edges from the root.
+    A malformed tree (parent[0] != -1 or parent[n] outside [0, n)) flags
+    ROW_BAD_TREE and gets an all-False mask and depth 0.
+
+    Input: parent int [B, N].  Returns dict(mask bool [B, N, N],
+    depth int64 [B, N], status [B]).
+    """
+    par = np.asarray(parent, np.int64)
+    B, N = par.shape
+    mask = np.zeros((B, N, N), bool)
+    depth = np.zeros((B, N), np.int64)
+    status = np.zeros(B, np.int64)
+    for b in range(B):
+        ok = par[b, 0] == -1 and all(0 <= par[b, n] < n for n in range(1, N))
+        if not ok:
+            status[b] = ROW_BAD_TREE
+            continue
+        for n in range(N):
+            cur, d = n, 0
+            while cur >= 0:
+                mask[b, n, cur] = True
+                cur = par[b, cur]
+                d += 1
+            depth[b, n] = d - 1
+    return dict(mask=mask, depth=depth, status=status)
