@@ -203,6 +203,21 @@ SV_API sv_status spec_draft_sample(const void *logits, sv_dtype dt, const float 
                                    float *out_probs, int32_t *out_row_status, void *workspace,
                                    size_t workspace_bytes, sv_stream_t stream);
 
+/*
+ * Token-tree attention mask (SpecInfer explainer, §技術の仕組み › 基本アイデア and
+ * §推論方法: all tree nodes are scored in one target pass, each node seeing
+ * itself and its ancestors only).
+ *  parent       int32 [B, N]: parent[0] = -1, 0 <= parent[n] < n.
+ *  out_mask     uint64 [B, N, W], W = ceil(N / 64): row n has bit m (bit
+ *               m % 64 of word m / 64) set iff m == n or m is an ancestor of n.
+ *  out_depth    nullable int32 [B, N]: edges from the root.
+ *  out_row_status nullable int32 [B]: SV_ROW_BAD_TREE for a malformed tree,
+ *               whose mask is all zero and depths 0.
+ *  Limits: 1 <= N <= SV_MAX_TREE_NODES.  No workspace.
+ */
+SV_API sv_status spec_tree_mask(const int32_t *parent, int B, int N, uint64_t *out_mask,
+                                int32_t *out_depth, int32_t *out_row_status, sv_stream_t stream);
+
 /* Static description of a status code; never NULL. */
 SV_API const char *spec_verify_status_string(sv_status s);
 

@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
             L.spec_draft_sample.argtypes = [_VP, _INT, _F32P, _F32P, _INT, _INT, _I32P, _F32P,
                                              _I32P, _VP, _SIZE, _VP]
             L.spec_draft_sample.restype = _INT
+            L.spec_tree_mask.argtypes = [_I32P, _INT, _INT, _VP, _I32P, _I32P, _VP]
+            L.spec_tree_mask.restype = _INT
             L.spec_verify_status_string.argtypes = [_INT]
             L.spec_verify_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -288,3 +290,26 @@ def spec_draft_sample(logits: torch.Tensor, temperatures: torch.Tensor, uniforms
     if st != 0:
         raise SpecVerifyError(st, "spec_draft_sample")
     return out_tokens, out_probs, out_row_status
+
+
+def spec_tree_mask(parent: torch.Tensor, out_mask=None, out_depth=None, out_row_status=None,
+                   stream=None):
+    """Ancestor mask of token trees (see spec_tree_mask in spec_verify.h).
+
+    parent int32 [B, N].  Returns (mask [B, N, ceil(N/64)] as int64 words
+    holding the uint64 bit rows, depth int32 [B, N], row_status int32 [B])."""
+    dev = parent.device
+    B, N = parent.shape
+    _check(parent, "parent", torch.int32, (B, N), dev)
+    W = (N + 63) // 64
+    if out_mask is None:
+        out_mask = torch.empty((B, N, W), dtype=torch.int64, device=dev)
+    if out_depth is None:
+        out_depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    if out_row_status is None:
+        out_row_status = torch.empty((B,), dtype=torch.int32, device=dev)
+    st = lib().spec_tree_mask(parent.data_ptr(), B, N, out_mask.data_ptr(), out_depth.data_ptr(),
+                              out_row_status.data_ptr(), _stream_ptr(dev, stream))
+    if st != 0:
+        raise SpecVerifyError(st, "spec_tree_mask")
+    return out_mask, out_depth, out_row_status
