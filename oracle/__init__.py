@@ -7,5 +7,5 @@ from .spec_verify_oracle import (  # noqa: F401
     ROW_OK, ROW_BAD_TOKEN, ROW_NONFINITE, ROW_BAD_TREE, ROW_TIMEOUT,
     ROW_BAD_TEMPERATURE, tempered_softmax, first_argmax, inverse_cdf,
     residual_distribution, verify_chain, verify_chain_greedy,
-    verify_tree_greedy, draft_sample, tree_ancestor_mask,
+    verify_tree_greedy, draft_sample, tree_ancestor_mask, tree_kv_compact,
 )

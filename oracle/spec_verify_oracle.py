@@ -448,3 +448,51 @@ def tree_ancestor_mask(parent):
                 d += 1
             depth[b, n] = d - 1
     return dict(mask=mask, depth=depth, status=status)
+
+
+# --------------------------------------------------------------------------
+# KV-cache compaction after tree verification
+# --------------------------------------------------------------------------
+
+def tree_kv_compact(kv, base, path, num_accepted):
+    """Keep the accepted path's KV rows of each tree, contiguous after the context.
+
+    [SpS] §実装のポイント: the KV cache entries of rejected tokens are discarded;
+    [SpecInfer] §推論方法: the tree's nodes were all scored in one pass, so
+    their KV rows sit in node order after the context.  Reading: tree node n
+    (1 <= n < N; node 0 is the context's last token) was written at slot
+    base[b] + n - 1; after the walk the accepted path nodes path[b, 0..d-1]
+    (d = num_accepted[b]) are moved to slots base[b] + 0..d-1, in path order,
+    and the cache length becomes base[b] + d.  Rows of slots outside those
+    moves are unchanged.  A row whose path is not a valid accepted path
+    (d outside [0, path width], a node id not above the previous one or below
+    i + 1, a slot outside the cache) flags ROW_BAD_TREE and moves nothing.
+
+    Inputs: kv [B, S, E] (any dtype), base int [B], path int [B, Wp],
+    num_accepted int [B].  Returns dict(kv (a new array), length [B], status [B]).
+    """
+    out = np.array(kv, copy=True)
+    B, S = out.shape[:2]
+    base = np.asarray(base, np.int64)
+    path = np.asarray(path, np.int64)
+    nacc = np.asarray(num_accepted, np.int64)
+    length = base.copy()
+    status = np.zeros(B, np.int64)
+    for b in range(B):
+        d = nacc[b]
+        ok = 0 <= d <= path.shape[1] and base[b] >= 0
+        prev = 0
+        for i in range(d if ok else 0):
+            p = path[b, i]
+            if p < i + 1 or p <= prev or base[b] + p - 1 >= S:
+                ok = False
+                break
+            prev = p
+        if not ok:
+            status[b] = ROW_BAD_TREE
+            continue
+        rows = [np.array(kv[b, base[b] + path[b, i] - 1], copy=True) for i in range(d)]
+        for i in range(d):
+            out[b, base[b] + i] = rows[i]
+        length[b] = base[b] + d
+    return dict(kv=out, length=length, status=status)
