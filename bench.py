@@ -43,7 +43,7 @@ from speculative_decoding_verification_48_gb300 import workloads as W  # noqa: E
 METRIC = "verified draft positions/sec and achieved HBM GB/s vs 8 TB/s (1 GB300)"
 # Rows of every bench workload start on 16-byte boundaries, so each call runs
 # the two-launch path (sv_stats_kernel, then sv_decide_kernel as its
-# programmatic dependent, after a control-block memset) unless
+# programmatic dependent; no memset) unless
 # SPEC_VERIFY_KERNEL=tile selects the register-tile kernels (two launches).
 _TILE = os.environ.get("SPEC_VERIFY_KERNEL", "").startswith("t")
 KERNEL_NAME = ("sv_verify_kernel (Phase-A + Phase-B launches)" if _TILE
@@ -103,10 +103,15 @@ def measured_peak():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the sources the timed chain kernels compile from: the bf16
+    translation unit, the host launch code and every header it includes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_48_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cuh", ".h")))
+    files += ["sv_api.cu", "sv_chain_bf16.cu"]
+    for f in files:
         h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "spec_verify.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -373,7 +378,44 @@ def other_workloads(sv, dev, stream, peak):
     out[tree.name] = {"us_per_call": ms * 1e3, "positions_per_s": tree.B * (tree.N - 1) / (ms * 1e-3),
                       "GBps": nbytes / (ms * 1e-3) / 1e9, "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
                       "algorithmic_bytes": nbytes, "l2": "flushed before each call (256 MB read)"}
-    del flush
+
+    def flushed(call, n=200):
+        ts = []
+        for _ in range(n):
+            with torch.cuda.stream(stream):
+                flush.sum()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return float(np.median(ts))
+
+    # the tree's attention mask for the same 16 trees of 64 nodes
+    mres = sv.spec_tree_mask(args[1], stream=stream)
+    ms = flushed(lambda: sv.spec_tree_mask(args[1], out_mask=mres[0], out_depth=mres[1],
+                                           out_row_status=mres[2], stream=stream))
+    mbytes = tree.B * tree.N * 4 + mres[0].numel() * 8 + mres[1].numel() * 4
+    out["tree_mask_B16_N64"] = {"us_per_call": ms * 1e3, "GBps": mbytes / (ms * 1e-3) / 1e9,
+                                "algorithmic_bytes": mbytes,
+                                "l2": "flushed before each call (256 MB read)"}
+    # KV compaction of the walked paths: a [32 layers, 16 trees, 4160 slots]
+    # cache of 4 KB slot rows (8 KV heads x 128 x K and V, bf16), context 4096
+    L_, S_, row = 32, 4096 + tree.N, 4096
+    kvc = torch.empty((L_ * tree.B, S_, row // 2), dtype=torch.bfloat16, device=dev)
+    kbase = torch.full((L_ * tree.B,), 4096, dtype=torch.int32, device=dev)
+    kpath = res[0].repeat(L_, 1).contiguous()
+    knacc = res[2].repeat(L_).contiguous()
+    kout = sv.spec_tree_kv_compact(kvc, kbase, kpath, knacc, stream=stream)
+    ms = flushed(lambda: sv.spec_tree_kv_compact(kvc, kbase, kpath, knacc, out_length=kout[0],
+                                                 out_row_status=kout[1], stream=stream))
+    kbytes = int(knacc.sum().item()) * row * 2
+    out["kv_compact_L32_B16_S4160_row4KB"] = {
+        "us_per_call": ms * 1e3, "GBps": kbytes / (ms * 1e-3) / 1e9,
+        "algorithmic_bytes": kbytes, "l2": "flushed before each call (256 MB read)"}
+    del kvc, flush
     return out
 
 

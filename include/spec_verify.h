@@ -218,6 +218,37 @@ SV_API sv_status spec_draft_sample(const void *logits, sv_dtype dt, const float 
 SV_API sv_status spec_tree_mask(const int32_t *parent, int B, int N, uint64_t *out_mask,
                                 int32_t *out_depth, int32_t *out_row_status, sv_stream_t stream);
 
+/*
+ * KV-cache compaction after token-tree verification ("論文解説: Speculative
+ * Sampling", §実装のポイント: the KV entries of rejected tokens are dropped;
+ * SpecInfer explainer, §推論方法: all tree nodes were scored in one pass, so
+ * their KV rows lie in node order after the context).  Tree node n >= 1 of
+ * tree b was written at slot base[b] + n - 1; the accepted path nodes
+ * path[b, 0..d-1] (d = num_accepted[b], the output of
+ * spec_verify_tree_greedy) move to slots base[b] + 0..d-1 in path order, in
+ * place, and the cache length becomes base[b] + d.  Other slots keep their
+ * bytes.
+ *  kv           device, [B, S] rows of row_bytes bytes each (any element
+ *               type: rows are moved as bytes), updated in place.  16-byte
+ *               aligned; row_bytes a positive multiple of 16.
+ *  base         int32 [B]: slot of tree node 1 (the first slot after the
+ *               context).
+ *  path         int32 [B, path_width], 1 <= path_width <= SV_MAX_TREE_DEPTH + 1.
+ *  num_accepted int32 [B].
+ *  out_length   nullable int32 [B]: base[b] + d, or base[b] for a bad row.
+ *  out_row_status nullable int32 [B]: SV_ROW_BAD_TREE when d is outside
+ *               [0, path_width], base[b] < 0, or a path entry is below i + 1,
+ *               not above the previous entry, or names a slot >= S; such a
+ *               row moves nothing.
+ *  All pointers are device pointers owned by the caller.  No workspace; the
+ *  call is asynchronous on `stream`.  Returns SV_ERR_INVALID_ARG for null
+ *  required pointers, bad sizes or misaligned buffers.
+ */
+SV_API sv_status spec_tree_kv_compact(void *kv, size_t row_bytes, int B, int S,
+                                      const int32_t *base, const int32_t *path, int path_width,
+                                      const int32_t *num_accepted, int32_t *out_length,
+                                      int32_t *out_row_status, sv_stream_t stream);
+
 /* Static description of a status code; never NULL. */
 SV_API const char *spec_verify_status_string(sv_status s);
 

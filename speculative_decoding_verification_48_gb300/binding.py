@@ -80,6 +80,9 @@ def lib() -> ctypes.CDLL:
             L.spec_draft_sample.restype = _INT
             L.spec_tree_mask.argtypes = [_I32P, _INT, _INT, _VP, _I32P, _I32P, _VP]
             L.spec_tree_mask.restype = _INT
+            L.spec_tree_kv_compact.argtypes = [_VP, _SIZE, _INT, _INT, _I32P, _I32P, _INT,
+                                               _I32P, _I32P, _I32P, _VP]
+            L.spec_tree_kv_compact.restype = _INT
             L.spec_verify_status_string.argtypes = [_INT]
             L.spec_verify_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -313,3 +316,34 @@ def spec_tree_mask(parent: torch.Tensor, out_mask=None, out_depth=None, out_row_
     if st != 0:
         raise SpecVerifyError(st, "spec_tree_mask")
     return out_mask, out_depth, out_row_status
+
+
+def spec_tree_kv_compact(kv: torch.Tensor, base: torch.Tensor, path: torch.Tensor,
+                         num_accepted: torch.Tensor, out_length=None, out_row_status=None,
+                         stream=None):
+    """Move each tree's accepted-path KV rows to contiguous slots, in place
+    (see spec_tree_kv_compact in spec_verify.h).
+
+    kv [B, S, ...] contiguous, any dtype, each [S] row a multiple of 16 bytes;
+    base, num_accepted int32 [B]; path int32 [B, Wp].  Returns (length [B],
+    row_status [B])."""
+    dev = kv.device
+    B, S = kv.shape[:2]
+    _check(kv, "kv", device=dev)
+    row_bytes = (kv.numel() // (B * S)) * kv.element_size() if B * S else 0
+    _check(base, "base", torch.int32, (B,), dev)
+    _check(num_accepted, "num_accepted", torch.int32, (B,), dev)
+    if path.dim() != 2 or path.shape[0] != B:
+        raise ValueError("path must be [B, Wp]")
+    _check(path, "path", torch.int32, tuple(path.shape), dev)
+    if out_length is None:
+        out_length = torch.empty((B,), dtype=torch.int32, device=dev)
+    if out_row_status is None:
+        out_row_status = torch.empty((B,), dtype=torch.int32, device=dev)
+    st = lib().spec_tree_kv_compact(kv.data_ptr(), row_bytes, B, S, base.data_ptr(),
+                                    path.data_ptr(), path.shape[1], num_accepted.data_ptr(),
+                                    out_length.data_ptr(), out_row_status.data_ptr(),
+                                    _stream_ptr(dev, stream))
+    if st != 0:
+        raise SpecVerifyError(st, "spec_tree_kv_compact")
+    return out_length, out_row_status
