@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["c3", "c5", "c2", "c1", "c4"], default="c3",
-                    help="c4 (token trees) is accepted in --ncu mode only")
+                    help="c4 (token trees: mask, greedy walk, KV compaction) is accepted in --ncu mode only")
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -514,10 +514,20 @@ def main():
     peak, peak_kind = measured_peak()
 
     if a.ncu and a.workload == "c4":
+        # the tree path of one decoding step: the ancestor mask of the 16
+        # trees of 64 nodes, the greedy walk, then the KV compaction of the
+        # walked paths in a [32 layers x 16 trees, 320 slots, 4 KB] cache
+        # (context 256: the moved rows are the same as at any context, and
+        # the cache stays under 1 GB for full profiler captures)
         tree = W.c4_tree_f16_v32000()
         targs = [t.to(dev) for t in (tree.node_logits, tree.parent, tree.node_tokens)]
+        kvc = torch.zeros((32 * tree.B, 256 + tree.N, 2048), dtype=torch.bfloat16, device=dev)
+        kbase = torch.full((32 * tree.B,), 256, dtype=torch.int32, device=dev)
         for _ in range(1 + a.warmup + a.steps):
-            sv.spec_verify_tree_greedy(*targs, tree.max_depth, stream=stream)
+            sv.spec_tree_mask(targs[1], stream=stream)
+            path, _, nacc, _ = sv.spec_verify_tree_greedy(*targs, tree.max_depth, stream=stream)
+            sv.spec_tree_kv_compact(kvc, kbase, path.repeat(32, 1).contiguous(),
+                                    nacc.repeat(32).contiguous(), stream=stream)
         torch.cuda.synchronize()
         return
     case = make_workload(a.workload, row0=rank_row0(rank))
