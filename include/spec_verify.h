@@ -25,14 +25,16 @@
  *    The library never allocates and never synchronises the host; work is
  *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *  - `workspace` is caller-owned device memory of at least
- *    spec_verify_workspace_bytes(...) bytes, 16-byte aligned, with no
- *    initialisation required.  Its first 4096 bytes hold library state
- *    between calls (work-claim counters, left zeroed by every call and
- *    stamped valid; a call that finds no valid stamp resets them itself).
- *    A caller that writes into those 4096 bytes between calls must zero
- *    them before the next call.  Calls that may overlap on the GPU need
- *    distinct workspaces; calls in stream order may share one, whatever
- *    their shapes.
+ *    spec_verify_workspace_bytes(...) bytes, 16-byte aligned.  Its first
+ *    4096 bytes hold library state between calls (work-claim counters, left
+ *    zeroed by every call and stamped valid; a call that finds no valid
+ *    stamp resets them itself).  Those 4096 bytes must be zero before the
+ *    first call on the memory, and again whenever the caller has used that
+ *    memory for anything else in between: recycled memory can hold a stale
+ *    valid stamp above non-zero counters, which the library cannot tell from
+ *    its own state.  The rest of the workspace needs no initialisation.
+ *    Calls that may overlap on the GPU need distinct workspaces; calls in
+ *    stream order may share one, whatever their shapes.
  *  - Each call enqueues its kernels as programmatic dependents
  *    (programmatic dependent launch) of the work before them in `stream`:
  *    the first kernel waits on the device for that work to complete before

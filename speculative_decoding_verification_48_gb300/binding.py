@@ -98,9 +98,10 @@ def spec_verify_workspace_bytes(B: int, rows_per_batch: int, V: int, dtype: int 
 
 
 # ---------------------------------------------------------------------------
-# Workspace cache: one buffer per (device, stream), grown on demand.  Each
-# library call zeroes the control block it needs, so calls of any shape in
-# stream order can share the buffer.
+# Workspace cache: one buffer per (device, stream), grown on demand.  The
+# library keeps the 4 KB state header of a workspace valid from call to call,
+# so calls of any shape in stream order can share the buffer; a new buffer's
+# header is zeroed once, before the first call that uses it.
 # ---------------------------------------------------------------------------
 
 _ws_cache: dict = {}
@@ -113,6 +114,10 @@ def workspace_for(device: torch.device, stream_ptr: int, nbytes: int) -> torch.T
         ws = _ws_cache.get(key)
         if ws is None or ws.numel() < nbytes:
             ws = torch.empty(max(nbytes, 4096), dtype=torch.uint8, device=device)
+            ws[:4096].zero_()
+            # the zero-fill ran on torch's current stream; the library call
+            # runs on `stream_ptr`, so finish the fill before handing it out
+            torch.cuda.current_stream(device).synchronize()
             _ws_cache[key] = ws
         return ws
 
