@@ -8,4 +8,6 @@ from .spec_verify_oracle import (  # noqa: F401
     ROW_BAD_TEMPERATURE, tempered_softmax, first_argmax, inverse_cdf,
     residual_distribution, verify_chain, verify_chain_greedy,
     verify_tree_greedy, draft_sample, tree_ancestor_mask, tree_kv_compact,
+    acceptance_probability, accepted_count_law, expected_tokens_per_round,
+    speedup_estimate,
 )

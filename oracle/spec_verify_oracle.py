@@ -496,3 +496,63 @@ def tree_kv_compact(kv, base, path, num_accepted):
             out[b, base[b] + i] = rows[i]
         length[b] = base[b] + d
     return dict(kv=out, length=length, status=status)
+
+
+# --------------------------------------------------------------------------
+# Rounds of speculative decoding (the multi-round model)
+# --------------------------------------------------------------------------
+
+def acceptance_probability(target_logits, draft_logits, T=1.0):
+    """Chance that a draft drawn from q passes the accept test: sum_x min(p(x), q(x)).
+
+    [SpS] §修正付き棄却サンプリング: a draft x ~ q is kept with probability
+    min(1, p(x)/q(x)), so it is kept with probability
+    sum_x q(x) min(1, p(x)/q(x)) = sum_x min(p(x), q(x)).  p and q are the
+    tempered softmaxes of the rows (T > 0).  Inputs [..., V]; returns [...].
+    """
+    target_logits = np.asarray(target_logits, np.float64)
+    T = np.broadcast_to(np.asarray(T, np.float64), target_logits.shape[:-1])
+    p = tempered_softmax(target_logits, T)
+    q = tempered_softmax(np.asarray(draft_logits, np.float64), T)
+    return np.minimum(p, q).sum(axis=-1)
+
+
+def accepted_count_law(alphas):
+    """Law of n_accepted in one round: P(n = k) for k = 0..gamma.
+
+    [SpS] §技術的詳細 ステップ3 and the listing's loop: drafts are tested in
+    order and the round stops at the first rejection, so with independent
+    per-position acceptance probabilities alpha_0..alpha_{gamma-1}
+    P(n = k) = alpha_0 ... alpha_{k-1} (1 - alpha_k) for k < gamma and
+    P(n = gamma) = alpha_0 ... alpha_{gamma-1}.  The round then commits
+    n + 1 tokens (the replacement or the bonus token, §期待される高速化).
+    """
+    a = np.asarray(alphas, np.float64)
+    g = a.shape[0]
+    law = np.empty(g + 1)
+    reach = 1.0
+    for k in range(g):
+        law[k] = reach * (1.0 - a[k])
+        reach *= a[k]
+    law[g] = reach
+    return law
+
+
+def expected_tokens_per_round(alphas):
+    """E[tokens committed per round] = sum_k (k + 1) P(n_accepted = k).
+
+    [SpS] §期待される高速化 gives (1 - alpha^(gamma+1)) / (1 - alpha) for a
+    constant alpha; this is the same expectation for per-position alphas.
+    """
+    law = accepted_count_law(alphas)
+    return float(np.dot(np.arange(1, law.shape[0] + 1), law))
+
+
+def speedup_estimate(tokens_per_round, gamma, c):
+    """Wall-clock speedup model of [SpS] §期待される高速化.
+
+    A round costs gamma draft forwards of relative cost c plus one target
+    forward, against one target forward per token without drafting:
+    speedup = E[tokens per round] / (1 + gamma c).
+    """
+    return float(tokens_per_round) / (1.0 + gamma * float(c))

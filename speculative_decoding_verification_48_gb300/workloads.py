@@ -348,3 +348,40 @@ def make_draft(name: str, seed: int, B: int, V: int, dtype: str = "bf16", target
         unif[i] = torch.rand(1, generator=g)[0]
         logits[i] = row.to(DTYPES[dtype])
     return DraftCase(name, logits, temps, unif, dict(seed=seed, dtype=dtype))
+
+
+@dataclass
+class AlphaPair:
+    """One target row and one draft row whose distributions overlap by a
+    known amount: sum_x min(p(x), q(x)) = alpha, where p and q are the
+    distributions the stored fp32 logits define at T = 1.
+
+    p is a random distribution, p(x) proportional to exp(N(0, sigma^2)),
+    stored as target logits log p.  q moves weight w of p onto the least
+    likely token k, q = (1 - w) p + w e_k, stored as draft logits log q.
+    The overlap of such a pair is 1 - w (1 - p(k)), so
+    w = (1 - alpha) / (1 - p(k)) gives alpha exactly; the fp32 rounding of
+    the stored logits moves it by about 1e-7.
+    """
+    target_logits: torch.Tensor    # fp32 [V]
+    draft_logits: torch.Tensor     # fp32 [V]
+    alpha: float
+    k: int
+    w: float
+
+
+def make_alpha_pair(seed: int, V: int, alpha: float, sigma: float = 1.5) -> AlphaPair:
+    if not 0.0 < alpha <= 1.0:
+        raise ValueError("alpha must lie in (0, 1]")
+    if V < 2:
+        raise ValueError("V must be at least 2")
+    g = gen_for(seed, 0xA1FA)
+    z = torch.randn(V, generator=g, dtype=torch.float64) * sigma
+    p = torch.exp(z - z.max())
+    p = p / p.sum()
+    k = int(torch.argmin(p))
+    w = (1.0 - alpha) / (1.0 - float(p[k]))
+    q = (1.0 - w) * p
+    q[k] += w
+    return AlphaPair(torch.log(p).to(torch.float32), torch.log(q).to(torch.float32),
+                     float(alpha), k, float(w))
