@@ -416,6 +416,18 @@ def other_workloads(sv, dev, stream, peak):
         "us_per_call": ms * 1e3, "GBps": kbytes / (ms * 1e-3) / 1e9,
         "algorithmic_bytes": kbytes, "l2": "flushed before each call (256 MB read)"}
     del kvc, flush
+    # multi-round simulation through the draft sampler and the chain verifier:
+    # 1024 sequences x 64 tokens, gamma = 4, a p / q pair of overlap 0.8, V = 32000
+    from speculative_decoding_verification_48_gb300 import simulate
+    with torch.cuda.stream(stream):
+        r = simulate.simulate(4, 0.8, sequences=1024, tokens=64, V=32000, c=0.05, seed=1,
+                              device=dev)
+    out["simulate_g4_alpha0.8_S1024_V32000_f32"] = {
+        "tokens_per_round": r.tokens_per_round, "tokens_per_round_se": r.tokens_per_round_se,
+        "model_tokens_per_round": r.model_tokens_per_round, "speedup_model_c0.05": r.speedup_model,
+        "rounds": r.rounds, "us_per_round": r.us_per_round,
+        "note": "us_per_round: device time between events around one draft-sample + verify "
+                "pair over all 1024 sequences, host launch gaps included"}
     return out
 
 

@@ -126,3 +126,15 @@ def test_binding_refuses_cpu_tensors():
     with pytest.raises((ValueError, RuntimeError)):
         binding.spec_verify_chain(x, torch.zeros(2, 2, 10), torch.zeros(2, 2, dtype=torch.int32),
                                   torch.ones(2), torch.zeros(2, 3))
+
+
+def test_simulator_host_checks():
+    """The simulator runs only the library's CUDA kernels: without a CUDA
+    device it refuses, before any work."""
+    from speculative_decoding_verification_48_gb300 import simulate
+    with pytest.raises(ValueError):
+        simulate.simulate(4, 0.8, device="cpu")
+    with pytest.raises(ValueError):
+        simulate.simulate(0, 0.8, device="cpu")
+    assert simulate._parse_gammas("1-4") == [1, 2, 3, 4]
+    assert simulate._parse_gammas("2,5") == [2, 5]
