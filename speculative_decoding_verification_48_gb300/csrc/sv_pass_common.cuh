@@ -167,6 +167,23 @@ __device__ __forceinline__ void vec_load(const typename Elt<DT>::T *p, float *o)
 
 // One raw vector of VEC elements of DT (8 or 16 bytes), loaded now and
 // unpacked when used.
+// Asynchronous copy of 8 or 16 bytes from global to shared memory (no
+// register staging); completion is per thread, after cp_async_wait_all.
+template <int BYTES>
+__device__ __forceinline__ void cp_async(void *smem, const void *gmem) {
+  const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  if constexpr (BYTES == 16)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
 template <int DT, int VEC> struct RawVec {
   static constexpr int kB = VEC * (int)sizeof(typename Elt<DT>::T);
   static_assert(kB == 16 || kB == 8, "vector loads are 8 or 16 bytes");

@@ -20,6 +20,8 @@ struct DecideSmem {
   float rowM[kMaxRows], rowZ[kMaxRows];
   int rowI[kMaxRows];
   int j, status, last;
+  // per warp: the p and q halves of one residual chunk, copied in by cp.async
+  alignas(16) unsigned char stage[kPassWarps][2 * kResidBytes];
 };
 
 struct TreeSmem {
@@ -201,21 +203,18 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   const DTy *qrow = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V;
   float *rs = P.resid + (size_t)b * P.cR;
   const int c0 = (int)((long long)h * P.cR / P.H), c1 = (int)((long long)(h + 1) * P.cR / P.H);
-  // each warp takes chunks c0 + warp, c0 + warp + 8, ..., with all loads of
-  // a chunk in flight before its first residual term
-  for (int ch = c0 + warp; ch < c1; ch += kPassWarps) {
-    const int x0 = ch * PC::kElems;
-    const int n = min(PC::kElems, V - x0);
-    RawVec<TDT, PC::kVec> ra[PC::kVecs];
-    RawVec<DDT, PC::kVec> rq[PC::kVecs];
-#pragma unroll
-    for (int u = 0; u < PC::kVecs; ++u) {
-      const int e = (lane + 32 * u) * PC::kVec;
-      if (e < n) {
-        ra[u].load(prow + x0 + e);
-        rq[u].load(qrow + x0 + e);
-      }
-    }
+  // Each warp takes chunk pairs (ch, ch + 8), ch = c0 + warp + 16 i: the
+  // first chunk is loaded into registers, the second is copied into this
+  // warp's shared-memory stage by cp.async, and both are in flight before the
+  // first residual term (one memory round trip per pair).  Every lane reads
+  // back only the vectors it copied itself, so its own wait suffices.
+  using RA = RawVec<TDT, PC::kVec>;
+  using RQ = RawVec<DDT, PC::kVec>;
+  typename RA::R *sa = reinterpret_cast<typename RA::R *>(sm.stage[warp]);
+  typename RQ::R *sq = reinterpret_cast<typename RQ::R *>(sm.stage[warp] + kResidBytes);
+  RA ra[PC::kVecs];
+  RQ rq[PC::kVecs];
+  auto chunk_sum = [&](int n) {
     unsigned long long s2 = 0ull;  // (+0, +0)
 #pragma unroll
     for (int u = 0; u < PC::kVecs; ++u) {
@@ -232,8 +231,51 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
       }
     }
     const float2 sp = f2_unpack(s2);
-    float s = warp_sum(sp.x + sp.y);
+    return warp_sum(sp.x + sp.y);
+  };
+  // 8-byte vectors (a 16-bit target beside fp32 draft rows) measured slower
+  // staged than one register-held chunk at a time, so only pairs of 16-byte
+  // vectors take the stage
+  constexpr bool kStage = RA::kB == 16 && RQ::kB == 16;
+  for (int ch = c0 + warp; ch < c1; ch += (kStage ? 2 : 1) * kPassWarps) {
+    const int chB = ch + kPassWarps;
+    const int nB = kStage && chB < c1 ? min(PC::kElems, V - chB * PC::kElems) : 0;
+    if (nB > 0) {
+      const int xB = chB * PC::kElems;
+#pragma unroll
+      for (int u = 0; u < PC::kVecs; ++u) {
+        const int e = (lane + 32 * u) * PC::kVec;
+        if (e < nB) {
+          cp_async<RA::kB>(sa + lane + 32 * u, prow + xB + e);
+          cp_async<RQ::kB>(sq + lane + 32 * u, qrow + xB + e);
+        }
+      }
+      cp_async_commit();
+    }
+    const int x0 = ch * PC::kElems;
+    const int n = min(PC::kElems, V - x0);
+#pragma unroll
+    for (int u = 0; u < PC::kVecs; ++u) {
+      const int e = (lane + 32 * u) * PC::kVec;
+      if (e < n) {
+        ra[u].load(prow + x0 + e);
+        rq[u].load(qrow + x0 + e);
+      }
+    }
+    const float s = chunk_sum(n);
     if (lane == 0) rs[ch] = s;
+    if (nB > 0) {
+      cp_async_wait_all();
+#pragma unroll
+      for (int u = 0; u < PC::kVecs; ++u) {
+        if ((lane + 32 * u) * PC::kVec < nB) {
+          ra[u].r = sa[lane + 32 * u];
+          rq[u].r = sq[lane + 32 * u];
+        }
+      }
+      const float sB = chunk_sum(nB);
+      if (lane == 0) rs[chB] = sB;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {
