@@ -327,10 +327,37 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
   __syncthreads();
   int flags = 0;
   const float2 *pb = P.part + (size_t)b * N * P.cMax;
-  for (int r = warp; r < N; r += kPassWarps) {
-    const float2 mi = warp_row_argmax(pb + (size_t)r * P.cMax, P.cT);
-    if (lane == 0) sm.a[r] = __float_as_int(mi.y);
-    if (isnan(mi.x)) flags |= SV_ROW_NONFINITE;
+  if (P.cT <= 32) {
+    // Rows of at most 32 chunks: each lane holds one chunk partial of each
+    // of 8 rows, all loaded at once, so a warp's group of 8 rows costs one
+    // memory round trip.  The merge is that of warp_row_argmax: the largest
+    // value, the lowest index among chunks holding it, NaN flags the row.
+    for (int r0 = warp * 8; r0 < N; r0 += kPassWarps * 8) {
+      float2 pt[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int r = r0 + k;
+        pt[k] = (r < N && lane < P.cT)
+                    ? __ldcg(pb + (size_t)r * P.cMax + lane)
+                    : make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int r = r0 + k;  // warp-uniform
+        if (r < N) {
+          if (__any_sync(0xffffffffu, isnan(pt[k].x))) flags |= SV_ROW_NONFINITE;
+          const float M = warp_max_nan(pt[k].x);
+          const int I = warp_min_int(pt[k].x == M ? __float_as_int(pt[k].y) : 0x7fffffff);
+          if (lane == 0) sm.a[r] = I;
+        }
+      }
+    }
+  } else {
+    for (int r = warp; r < N; r += kPassWarps) {
+      const float2 mi = warp_row_argmax(pb + (size_t)r * P.cMax, P.cT);
+      if (lane == 0) sm.a[r] = __float_as_int(mi.y);
+      if (isnan(mi.x)) flags |= SV_ROW_NONFINITE;
+    }
   }
   for (int n = threadIdx.x; n < N; n += kPassThreads) {
     const int par = __ldg(P.parent + (size_t)b * N + n);

@@ -400,3 +400,25 @@ def test_gpu_expected_tokens_constant_alpha(sv):
     emitted = nacc.cpu().numpy() + 1
     want = (1 - alpha ** (g + 1)) / (1 - alpha)
     assert abs(emitted.mean() - want) < 4 * emitted.std() / np.sqrt(n)
+
+
+@pytest.mark.parametrize("V,N,B,dtype,D", [(704, 1024, 3, "f16", 31), (70000, 40, 2, "f16", 8),
+                                           (20000, 64, 5, "f32", 8), (32000, 64, 6, "bf16", 6)])
+def test_tree_aligned_rows(sv, V, N, B, dtype, D):
+    """Rows on 16-byte boundaries take the streaming pair: node-row merges of
+    at most 32 chunks (grouped per warp) and of more (V = 70000 fp16)."""
+    check_tree(sv, W.make_tree(f"tree_al_{V}", 4300 + V % 97, B=B, N=N, V=V, max_depth=D,
+                               kmin=1, kmax=3, dtype=dtype, p_match=0.9))
+
+
+def test_tree_errors_aligned_rows(sv):
+    case = W.make_tree("err_al", 4400, B=4, N=48, V=4096, max_depth=8, p_match=1.0)
+    par = case.parent.clone()
+    tok = case.node_tokens.clone()
+    lg = case.node_logits.clone()
+    par[0, 9] = 30                   # parent after child
+    tok[1, 4] = -2                   # token out of range
+    lg[2, 40, 1000] = float("nan")   # NaN node row
+    lg[3, 7, :] = float("-inf")      # an all -inf node row: argmax at index 0
+    ref = check_tree(sv, W.TreeCase("err_al", lg, par, tok, 8))
+    assert ref["status"][0] & 4 and ref["status"][1] & 1 and ref["status"][2] & 2
