@@ -279,10 +279,13 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned prev = atomicAdd(P.done + b, 1u);
+    // one acquire-release add: it publishes this CTA's chunk sums (ordered
+    // before it by the barrier above) and, in the last CTA, acquires the
+    // other CTAs' sums
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                 : "=r"(prev) : "l"(P.done + b) : "memory");
     sm.last = (prev == (unsigned)P.H - 1u);
-    if (sm.last) __threadfence();
   }
   __syncthreads();
   if (!sm.last || warp != 0) return;
