@@ -277,7 +277,7 @@ __device__ __forceinline__ float2 softmax_merge(float2 a, float2 b, float c) {
 // Merge of one softmax row's `cnt` chunk partials by the whole warp: lanes
 // take chunks lane, lane + 32, ... (eight loads in flight per lane), then the
 // lane results are combined.  Returns (M, Z) with Z = sum_x 2^((x - M) c).
-__device__ __forceinline__ float2 warp_row_softmax(const float2 *part, int cnt, float c) {
+static __device__ __noinline__ float2 warp_row_softmax(const float2 *part, int cnt, float c) {
   const int lane = lane_id();
   float2 acc = make_float2(-CUDART_INF_F, 0.f);
   for (int i0 = 0; i0 < cnt; i0 += 256) {
@@ -323,7 +323,7 @@ __device__ __forceinline__ void warp_rows_softmax2(const float2 *pa, int ca, con
 // Merge of one argmax row's chunk partials (value, global first index): the
 // largest value, and the lowest index among chunks holding it.  NaN anywhere
 // gives a NaN value.
-__device__ __forceinline__ float2 warp_row_argmax(const float2 *part, int cnt) {
+static __device__ __noinline__ float2 warp_row_argmax(const float2 *part, int cnt) {
   const int lane = lane_id();
   float best = -CUDART_INF_F;
   int idx = 0x7fffffff;

@@ -31,7 +31,10 @@ struct TreeSmem {
 };
 
 // Writes an invalid row: every token (and path entry) -1, no draft accepted.
-__device__ __forceinline__ void pass_error_row(const PassParams &P, int b, int status, int width,
+// Out of line, like the other paths a verifying row rarely takes: the decide
+// kernel's common path then lies in fewer instruction-cache lines, which
+// matters because each call's logit stream evicts its code from L2.
+static __device__ __noinline__ void pass_error_row(const PassParams &P, int b, int status, int width,
                                                int32_t *tok, int32_t *path) {
   for (int s = lane_id(); s < width; s += 32) {
     tok[s] = -1;

@@ -178,7 +178,7 @@ __device__ __forceinline__ int warp_chunk_cross(int cnt, WF wf, float u, float &
 // s_i 2^((m_i - M) c) locate the crossing chunk of u * R, then that chunk is
 // rescanned element by element.  Returns a vocabulary index.
 template <int DT>
-__device__ int warp_sample_softmax_row(const typename Elt<DT>::T *row, const float2 *part, int cnt,
+static __device__ __noinline__ int warp_sample_softmax_row(const typename Elt<DT>::T *row, const float2 *part, int cnt,
                                        int V, float M, float c, float u) {
   using C = Chunk<DT>;
   constexpr int HALF = C::kElems / 2, PER = HALF / 32;
