@@ -251,6 +251,24 @@ SV_API sv_status spec_tree_kv_compact(void *kv, size_t row_bytes, int B, int S,
                                       const int32_t *num_accepted, int32_t *out_length,
                                       int32_t *out_row_status, sv_stream_t stream);
 
+/*
+ * Diagnostics.  Runs one of the library's bounded device-side waits on a flag
+ * that nothing sets, so that a caller can check that the wait gives up after
+ * its bound and reports instead of hanging (the verification calls report the
+ * same event as SV_ROW_TIMEOUT in out_row_status).
+ *  which        0: the stats kernel's wait for its claim counters to be reset
+ *               (a spin bound, about a second);
+ *               1: the register-tile kernels' wait for a row's decision flag
+ *               (2e9 clock cycles, about a second).
+ *  scratch      device memory of at least 64 bytes, 16-byte aligned; the call
+ *               zeroes and uses it.
+ *  out_status   device int32 [1]: SV_ROW_TIMEOUT when the wait ran out, the
+ *               expected result; SV_ROW_OK if the flag was seen.
+ * Takes about a second of GPU time.  The context stays usable afterwards.
+ */
+SV_API sv_status spec_verify_wait_selftest(int which, void *scratch, int32_t *out_status,
+                                           sv_stream_t stream);
+
 /* Static description of a status code; never NULL. */
 SV_API const char *spec_verify_status_string(sv_status s);
 

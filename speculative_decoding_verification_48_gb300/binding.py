@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
             L.spec_tree_kv_compact.argtypes = [_VP, _SIZE, _INT, _INT, _I32P, _I32P, _INT,
                                                _I32P, _I32P, _I32P, _VP]
             L.spec_tree_kv_compact.restype = _INT
+            L.spec_verify_wait_selftest.argtypes = [_INT, _VP, _I32P, _VP]
+            L.spec_verify_wait_selftest.restype = _INT
             L.spec_verify_status_string.argtypes = [_INT]
             L.spec_verify_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -352,3 +354,19 @@ def spec_tree_kv_compact(kv: torch.Tensor, base: torch.Tensor, path: torch.Tenso
     if st != 0:
         raise SpecVerifyError(st, "spec_tree_kv_compact")
     return out_length, out_row_status
+
+
+def spec_verify_wait_selftest(which: int, device=None, stream=None) -> int:
+    """Run bounded wait ``which`` (0: counter reset, 1: decision flag) on a
+    flag that nothing sets (see spec_verify_wait_selftest in spec_verify.h);
+    returns the status the device reported, SV_ROW_TIMEOUT when the wait gave
+    up as it should."""
+    dev = torch.device(device) if device is not None else torch.device("cuda")
+    scratch = torch.empty(64, dtype=torch.uint8, device=dev)
+    out = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    sp = _stream_ptr(dev, stream)
+    st = lib().spec_verify_wait_selftest(int(which), scratch.data_ptr(), out.data_ptr(), sp)
+    if st != 0:
+        raise SpecVerifyError(st, "spec_verify_wait_selftest")
+    torch.cuda.synchronize(dev)
+    return int(out.item())

@@ -23,7 +23,8 @@ LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libspec_verify.so")
 
 SOURCES = ["sv_api.cu", "sv_chain_f32.cu", "sv_chain_bf16.cu", "sv_chain_f16.cu",
-           "sv_greedy_tree.cu", "sv_no_alloc.cu", "sv_tree_mask.cu", "sv_kv_compact.cu"]
+           "sv_greedy_tree.cu", "sv_no_alloc.cu", "sv_tree_mask.cu", "sv_kv_compact.cu",
+           "sv_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

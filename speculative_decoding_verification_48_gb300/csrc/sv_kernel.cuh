@@ -83,6 +83,21 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
   return v;
 }
 
+// Bounded wait for a flag that another CTA sets: its value, or 0 once
+// kWaitCycles clock cycles (about a second) have passed without it.
+__device__ __forceinline__ unsigned wait_flag_bounded(const unsigned *flag) {
+  unsigned f = ld_acquire(flag);
+  if (!f) {
+    const long long t0 = clock64();
+    while (!f) {
+      __nanosleep(200);
+      f = ld_acquire(flag);
+      if (!f && clock64() - t0 > kWaitCycles) break;
+    }
+  }
+  return f;
+}
+
 __device__ __forceinline__ void st_release(unsigned *p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -852,15 +867,7 @@ __device__ void run_unit_B(const KParams &P, int b, int t, SmemChain &sm) {
   using TT = typename Elt<TDT>::T;
   using DTy = typename Elt<DDT>::T;
   if (threadIdx.x == 0) {
-    unsigned f = ld_acquire(P.flag + b);
-    if (!f) {
-      const long long t0 = clock64();
-      while (!f) {
-        __nanosleep(200);
-        f = ld_acquire(P.flag + b);
-        if (!f && clock64() - t0 > kWaitCycles) break;
-      }
-    }
+    const unsigned f = wait_flag_bounded(P.flag + b);
     sm.flag = f ? 1 : 0;
     if (f) {
       const Decision *d = P.dec + b;
