@@ -422,3 +422,35 @@ def test_tree_errors_aligned_rows(sv):
     lg[3, 7, :] = float("-inf")      # an all -inf node row: argmax at index 0
     ref = check_tree(sv, W.TreeCase("err_al", lg, par, tok, 8))
     assert ref["status"][0] & 4 and ref["status"][1] & 1 and ref["status"][2] & 2
+
+
+def test_chain_maximum_vocabulary(sv):
+    """V = 2^26, the library's limit: 32768 stats chunks and 65536 residual
+    chunks per bf16 row, so the long-row merge and the streamed crossing
+    search run.  Row 0 drafts the draft row's top token; row 1 drafts a token
+    far down the target's order, a rejection with a residual draw over all
+    2^26 entries.  Draft tokens are chosen here (a categorical draw over 2^26
+    entries is beyond the input generator's sampler)."""
+    V = 1 << 26
+    g = torch.Generator().manual_seed(2026)
+    bias = W.zipf_bias(2026, V)
+    tgt = (torch.randn((2, 2, V), generator=g) + bias).to(torch.bfloat16)
+    dft = (tgt[:, :1].float() + 0.5 * torch.randn((2, 1, V), generator=g)).to(torch.bfloat16)
+    toks = torch.empty((2, 1), dtype=torch.int32)
+    toks[0, 0] = int(torch.argmax(dft[0, 0].float()))
+    toks[1, 0] = int(torch.argmin(tgt[1, 0].float() - dft[1, 0].float()))
+    case = W.ChainCase("max_vocab", tgt, dft, False, toks,
+                       torch.tensor([0.9, 1.1], dtype=torch.float32),
+                       torch.tensor([[0.3, 0.77], [0.999, 0.41]], dtype=torch.float32))
+    cmp, ref, _ = check_chain(sv, case)
+    assert ref["num_accepted"][1] == 0           # the far-down draft is rejected
+
+
+def test_chain_large_batch(sv):
+    """4096 batch rows of short aligned rows: one decide CTA per row, a
+    decide grid far larger than one wave, every row checked."""
+    case = W.make_chain("large_batch", 4500, B=4096, gamma=3, V=1024, dtype="bf16",
+                        draft_sigma=(0.2, 2.0),
+                        temperature=lambda b, v: 0.0 if b % 5 == 0 else 0.3 + 1.2 * v)
+    cmp, ref, _ = check_chain(sv, case)
+    assert len(set(ref["num_accepted"].tolist())) == 4
