@@ -65,6 +65,11 @@ static void fill_workspace(KParams &P, void *ws, const Layout &L) {
   P.tiles = L.tiles;
 }
 
+unsigned long long next_call_id() {
+  static std::atomic<unsigned long long> calls{0};
+  return calls.fetch_add(1, std::memory_order_relaxed) + 1;
+}
+
 }  // namespace sv
 
 using namespace sv;

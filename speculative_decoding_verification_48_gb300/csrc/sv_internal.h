@@ -123,4 +123,8 @@ int sm_count(int device);
 // Workspace bytes covering both kernel families for the given shape.
 size_t workspace_bytes_any(int B, int rows, int V);
 
+// Identifier of a launched call, unique across every entry point and
+// instantiation of this process, never 0.
+unsigned long long next_call_id();
+
 }  // namespace sv

@@ -117,17 +117,20 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   S.claim_err = reinterpret_cast<unsigned long long *>(w + L.err);
   S.claim_ready = reinterpret_cast<unsigned long long *>(w + L.ready);
   S.claim_stamp = reinterpret_cast<unsigned long long *>(w + L.stamp);
-  {
-    static std::atomic<unsigned long long> calls{0};
-    S.call_id = calls.fetch_add(1, std::memory_order_relaxed) + 1;  // never 0
-  }
+  S.call_id = next_call_id();                    // never 0, unique in the process
+  S.part_tag = (unsigned)(S.call_id << 1) | 1u;  // odd: never a zeroed word's
   S.done = reinterpret_cast<unsigned *>(w + L.done);
-  S.part = reinterpret_cast<float2 *>(w + L.part);
+  S.part = reinterpret_cast<Part *>(w + L.part);
   S.resid = reinterpret_cast<float *>(w + L.resid);
   const long long want = (total + kPassWarps - 1) / kPassWarps;
   const long long cap = (long long)sms * occ;
   int grid = (int)(want < cap ? want : cap);
   if (grid < 1) grid = 1;
+  // Merging as partials arrive pays off when the stats work is many times
+  // what its resident warps hold: the decide CTAs then only become resident
+  // in the stats kernel's tail.  On a small call they would be resident
+  // from the start and poll through the whole stats kernel.
+  S.poll = total >= 16LL * grid * kPassWarps;
   // Both kernels are programmatic dependents of the work before them: the
   // stats kernel of whatever the stream ran last (it waits on the device
   // before touching the workspace), the decide kernel of the stats kernel.

@@ -28,6 +28,7 @@ constexpr int kClaimStripes = 16;  // stats-kernel claim counters
 constexpr int kClaimStride = 32;   // 128 bytes between counters
 constexpr int kClaimProbes = 4096; // bound of the end-of-work probe loop
 constexpr long long kReadySpins = 4000000;  // bound of the counter-reset wait (about a second)
+constexpr int kPollSpins = 512;     // rounds of partial polling before the dependency wait
 constexpr unsigned long long kStampValid = 0x5356434c41494d30ull;
 
 template <int DT> struct Chunk {
@@ -66,6 +67,15 @@ __device__ __forceinline__ unsigned fdiv(unsigned n, const FastDiv &f) {
   return (__umulhi(n, f.m) + n) >> f.l;
 }
 
+// A warp-chunk partial: two values (max and scaled sum of a softmax chunk,
+// or value and first index of an argmax chunk), each in its own 64-bit word
+// with the call's tag in the high half.  Each word is written by one 64-bit
+// store, so a reader that finds the tag in both words holds both values of
+// this call, without waiting for the whole stats grid.
+struct Part {
+  unsigned long long a, b;
+};
+
 struct PassParams {
   const void *target;  // chain: [B, gamma+1, V]; tree: [B*N, V]
   const void *draft;   // [B, gamma, V] logits or fp32 probabilities
@@ -89,7 +99,9 @@ struct PassParams {
                                     // previous call's decide kernel)
   unsigned long long call_id;       // unique per call, never 0
   unsigned *done;    // [B] residual-sweep arrivals
-  float2 *part;      // [B][rows][cMax] warp-chunk partials
+  Part *part;        // [B][rows][cMax] warp-chunk partials
+  unsigned part_tag; // odd, from call_id: marks this call's partials
+  int poll;          // 1: the decide kernel merges as partials arrive (large calls)
   float *resid;      // [B][cR] residual mass per chunk of the rejected row pair
 };
 
@@ -117,7 +129,7 @@ inline PassLayout make_pass_layout(int B, int rows, int V, int esT, int esD, boo
   L.stamp = L.ready + 128;
   size_t off = kPassHeaderBytes;
   L.done = off;  off = align_up(off + (size_t)B * 4, 256);
-  L.part = off;  off = align_up(off + (size_t)B * rows * L.cMax * sizeof(float2), 256);
+  L.part = off;  off = align_up(off + (size_t)B * rows * L.cMax * sizeof(Part), 256);
   L.resid = off; off = align_up(off + (size_t)B * L.cR * sizeof(float), 256);
   L.total = off;
   return L;
@@ -265,6 +277,29 @@ __device__ __forceinline__ void grid_dependents_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+__device__ __forceinline__ unsigned long long part_word(float v, unsigned tag) {
+  return ((unsigned long long)tag << 32) | __float_as_uint(v);
+}
+__device__ __forceinline__ void part_store(Part *p, float x, float y, unsigned tag) {
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(part_word(x, tag)),
+               "l"(part_word(y, tag))
+               : "memory");
+}
+// The values of a partial read after the dependency wait (complete by then).
+__device__ __forceinline__ float2 part_value(const Part *p) {
+  const ulonglong2 w = __ldcg(reinterpret_cast<const ulonglong2 *>(p));
+  return make_float2(__uint_as_float((unsigned)w.x), __uint_as_float((unsigned)w.y));
+}
+// One poll of a partial that may still be written.
+__device__ __forceinline__ void part_poll(const Part *p, unsigned long long &a,
+                                          unsigned long long &b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ bool part_tagged(unsigned long long a, unsigned long long b,
+                                            unsigned tag) {
+  return (unsigned)(a >> 32) == tag && (unsigned)(b >> 32) == tag;
+}
+
 // Softmax merge of two partials (m, s), s = sum 2^((x - m) c).  -inf maxima
 // carry no mass; NaN anywhere gives NaN.
 __device__ __forceinline__ float2 softmax_merge(float2 a, float2 b, float c) {
@@ -277,7 +312,7 @@ __device__ __forceinline__ float2 softmax_merge(float2 a, float2 b, float c) {
 // Merge of one softmax row's `cnt` chunk partials by the whole warp: lanes
 // take chunks lane, lane + 32, ... (eight loads in flight per lane), then the
 // lane results are combined.  Returns (M, Z) with Z = sum_x 2^((x - M) c).
-static __device__ __noinline__ float2 warp_row_softmax(const float2 *part, int cnt, float c) {
+static __device__ __noinline__ float2 warp_row_softmax(const Part *part, int cnt, float c) {
   const int lane = lane_id();
   float2 acc = make_float2(-CUDART_INF_F, 0.f);
   for (int i0 = 0; i0 < cnt; i0 += 256) {
@@ -285,7 +320,7 @@ static __device__ __noinline__ float2 warp_row_softmax(const float2 *part, int c
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int i = i0 + lane + 32 * k;
-      pt[k] = i < cnt ? __ldcg(part + i) : make_float2(-CUDART_INF_F, 0.f);
+      pt[k] = i < cnt ? part_value(part + i) : make_float2(-CUDART_INF_F, 0.f);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc = softmax_merge(acc, pt[k], c);
@@ -297,15 +332,15 @@ static __device__ __noinline__ float2 warp_row_softmax(const float2 *part, int c
 
 // Two softmax rows merged by one warp with the loads of both in flight at
 // once (each row at most 256 chunks); `pb2` may be null.
-__device__ __forceinline__ void warp_rows_softmax2(const float2 *pa, int ca, const float2 *pb2,
+__device__ __forceinline__ void warp_rows_softmax2(const Part *pa, int ca, const Part *pb2,
                                                    int cb, float c, float2 &ra, float2 &rb) {
   const int lane = lane_id();
   float2 xa[8], xb[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int i = lane + 32 * k;
-    xa[k] = i < ca ? __ldcg(pa + i) : make_float2(-CUDART_INF_F, 0.f);
-    xb[k] = (pb2 && i < cb) ? __ldcg(pb2 + i) : make_float2(-CUDART_INF_F, 0.f);
+    xa[k] = i < ca ? part_value(pa + i) : make_float2(-CUDART_INF_F, 0.f);
+    xb[k] = (pb2 && i < cb) ? part_value(pb2 + i) : make_float2(-CUDART_INF_F, 0.f);
   }
   float2 aa = make_float2(-CUDART_INF_F, 0.f), ab = aa;
 #pragma unroll
@@ -320,10 +355,62 @@ __device__ __forceinline__ void warp_rows_softmax2(const float2 *pa, int ca, con
   rb = make_float2(Mb, warp_sum(zb));
 }
 
+// warp_rows_softmax2 for rows of at most 64 chunks, run before the
+// dependency wait: each lane holds up to two chunk partials of each row and
+// re-reads those that do not carry this call's tag yet, at most `spins`
+// rounds.  True, with the merged rows, once every partial carries the tag;
+// false if the bound ran out (the caller then waits and merges again).
+__device__ __forceinline__ bool warp_rows_softmax2_poll(const Part *pa, int ca, const Part *pb2,
+                                                        int cb, float c, unsigned tag,
+                                                        int spins, float2 &ra, float2 &rb) {
+  const int lane = lane_id();
+  unsigned long long wa[2][2], wb[2][2];
+  bool na[2], nb[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    na[k] = lane + 32 * k < ca;
+    nb[k] = pb2 != nullptr && lane + 32 * k < cb;
+    wa[k][0] = wa[k][1] = wb[k][0] = wb[k][1] = 0ull;
+  }
+  for (int it = 0;; ++it) {
+    bool pending = false;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (na[k]) part_poll(pa + lane + 32 * k, wa[k][0], wa[k][1]);
+      if (nb[k]) part_poll(pb2 + lane + 32 * k, wb[k][0], wb[k][1]);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      na[k] = na[k] && !part_tagged(wa[k][0], wa[k][1], tag);
+      nb[k] = nb[k] && !part_tagged(wb[k][0], wb[k][1], tag);
+      pending |= na[k] || nb[k];
+    }
+    if (!__any_sync(0xffffffffu, pending)) break;
+    if (it >= spins) return false;
+    __nanosleep(128);
+  }
+  float2 aa = make_float2(-CUDART_INF_F, 0.f), ab = aa;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    if (lane + 32 * k < ca)
+      aa = softmax_merge(aa, make_float2(__uint_as_float((unsigned)wa[k][0]),
+                                         __uint_as_float((unsigned)wa[k][1])), c);
+    if (pb2 != nullptr && lane + 32 * k < cb)
+      ab = softmax_merge(ab, make_float2(__uint_as_float((unsigned)wb[k][0]),
+                                         __uint_as_float((unsigned)wb[k][1])), c);
+  }
+  const float Ma = warp_max_nan(aa.x), Mb = warp_max_nan(ab.x);
+  const float za = (aa.x == -CUDART_INF_F) ? 0.f : aa.y * ex2((aa.x - Ma) * c);
+  const float zb = (ab.x == -CUDART_INF_F) ? 0.f : ab.y * ex2((ab.x - Mb) * c);
+  ra = make_float2(Ma, warp_sum(za));
+  rb = make_float2(Mb, warp_sum(zb));
+  return true;
+}
+
 // Merge of one argmax row's chunk partials (value, global first index): the
 // largest value, and the lowest index among chunks holding it.  NaN anywhere
 // gives a NaN value.
-static __device__ __noinline__ float2 warp_row_argmax(const float2 *part, int cnt) {
+static __device__ __noinline__ float2 warp_row_argmax(const Part *part, int cnt) {
   const int lane = lane_id();
   float best = -CUDART_INF_F;
   int idx = 0x7fffffff;
@@ -333,7 +420,7 @@ static __device__ __noinline__ float2 warp_row_argmax(const float2 *part, int cn
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int i = i0 + lane + 32 * k;
-      pt[k] = i < cnt ? __ldcg(part + i) : make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
+      pt[k] = i < cnt ? part_value(part + i) : make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {

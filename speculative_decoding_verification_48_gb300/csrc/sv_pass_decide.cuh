@@ -85,9 +85,39 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
       ui = __ldg(P.unif + (size_t)b * G1 + i);
     }
   }
-  grid_dependency_wait();
+  // 1a. Softmax rows of at most 64 chunks are merged as their partials
+  // arrive, without waiting for the whole stats grid: every partial of the
+  // row pair must carry this call's tag (bounded polling; if the bound runs
+  // out, the block falls back to the wait and merges again).  A tagged
+  // partial was written after the stats kernel's own wait, so the work
+  // before this call is complete; the fence orders this kernel's later
+  // writes after that observation.
+  const int nrows = greedy ? G1 : (PROBS ? G1 : 2 * g + 1);
+  const Part *pb = P.part + (size_t)b * P.rows * P.cMax;
+  bool polled = false;
+  if (P.poll && !badT && !greedy && P.cT <= 64 && (PROBS || P.cD <= 64)) {
+    bool ok = true;
+    for (int r = warp; r < nrows; r += 2 * kPassWarps) {
+      const int r2 = r + kPassWarps;
+      const int ca = r < G1 ? P.cT : P.cD, cb = r2 < G1 ? P.cT : P.cD;
+      float2 za, zb = make_float2(0.f, 0.f);
+      ok = warp_rows_softmax2_poll(pb + (size_t)r * P.cMax, ca,
+                                   r2 < nrows ? pb + (size_t)r2 * P.cMax : nullptr, cb, c,
+                                   P.part_tag, kPollSpins, za, zb);
+      if (!ok) break;
+      if (lane == 0) {
+        sm.rowM[r] = za.x; sm.rowZ[r] = za.y;
+        if (r2 < nrows) { sm.rowM[r2] = zb.x; sm.rowZ[r2] = zb.y; }
+      }
+    }
+    polled = __syncthreads_and(ok);
+    if (polled) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+  }
   bool claim_err = false;
-  if (warp == 0) claim_err = __ldcg(P.claim_err) == P.call_id;
+  if (!polled) {
+    grid_dependency_wait();
+    if (warp == 0) claim_err = __ldcg(P.claim_err) == P.call_id;
+  }
   if (badT) {
     if (warp == 0) {
       pass_error_row(P, b, SV_ROW_BAD_TEMPERATURE, G1, ot, nullptr);
@@ -97,10 +127,9 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     }
     return;
   }
-  // 1. row merges: each warp takes rows warp, warp + 8, ... two at a time
-  const int nrows = greedy ? G1 : (PROBS ? G1 : 2 * g + 1);
-  const float2 *pb = P.part + (size_t)b * P.rows * P.cMax;
-  for (int r = warp; r < nrows; r += 2 * kPassWarps) {
+  // 1b. otherwise, after the wait: each warp takes rows warp, warp + 8, ...
+  // two at a time
+  for (int r = warp; !polled && r < nrows; r += 2 * kPassWarps) {
     const int r2 = r + kPassWarps;
     const int ca = r < G1 ? P.cT : P.cD, cb = r2 < G1 ? P.cT : P.cD;
     if (greedy) {
@@ -183,7 +212,7 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     if (greedy) {
       tok_j = sm.rowI[j];
     } else {
-      const float2 *pr = pb + (size_t)g * P.cMax;
+      const Part *pr = pb + (size_t)g * P.cMax;
       tok_j = warp_sample_softmax_row<TDT>(tgt + (size_t)g * V, pr, P.cT, V, sm.rowM[g], c,
                                            ug);
     }
@@ -282,6 +311,10 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   }
   __syncthreads();
   if (threadIdx.x == 0) {
+    // a block that merged by polling waits here: the stats kernel zeroes
+    // done[] before its first partial, and the stats grid has long finished
+    // by now, so this returns at once
+    if (polled) grid_dependency_wait();
     // one acquire-release add: it publishes this CTA's chunk sums (ordered
     // before it by the barrier above) and, in the last CTA, acquires the
     // other CTAs' sums
@@ -332,7 +365,7 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
   if (threadIdx.x == 0) sm.flags = 0;
   __syncthreads();
   int flags = 0;
-  const float2 *pb = P.part + (size_t)b * N * P.cMax;
+  const Part *pb = P.part + (size_t)b * N * P.cMax;
   if (P.cT <= 32) {
     // Rows of at most 32 chunks: each lane holds one chunk partial of each
     // of 8 rows, all loaded at once, so a warp's group of 8 rows costs one
@@ -344,7 +377,7 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
       for (int k = 0; k < 8; ++k) {
         const int r = r0 + k;
         pt[k] = (r < N && lane < P.cT)
-                    ? __ldcg(pb + (size_t)r * P.cMax + lane)
+                    ? part_value(pb + (size_t)r * P.cMax + lane)
                     : make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
       }
 #pragma unroll
@@ -421,7 +454,7 @@ __device__ void decide_draft_row(const PassParams &P, int b) {
   const int lane = lane_id(), V = P.V;
   const float T = __ldg(P.temps + b);
   const TT *row = reinterpret_cast<const TT *>(P.target) + (size_t)b * V;
-  const float2 *pr = P.part + (size_t)b * P.cMax;
+  const Part *pr = P.part + (size_t)b * P.cMax;
   int status = 0, tok = -1;
   float prob = 0.f;
   if (bad_temperature(T)) {

@@ -178,12 +178,12 @@ __device__ __forceinline__ int warp_chunk_cross(int cnt, WF wf, float u, float &
 // s_i 2^((m_i - M) c) locate the crossing chunk of u * R, then that chunk is
 // rescanned element by element.  Returns a vocabulary index.
 template <int DT>
-static __device__ __noinline__ int warp_sample_softmax_row(const typename Elt<DT>::T *row, const float2 *part, int cnt,
+static __device__ __noinline__ int warp_sample_softmax_row(const typename Elt<DT>::T *row, const Part *part, int cnt,
                                        int V, float M, float c, float u) {
   using C = Chunk<DT>;
   constexpr int HALF = C::kElems / 2, PER = HALF / 32;
   auto wt = [&](int i) {
-    const float2 p = __ldcg(part + i);
+    const float2 p = part_value(part + i);
     return p.x != -CUDART_INF_F ? p.y * ex2((p.x - M) * c) : 0.f;
   };
   float R = 0.f, base = 0.f;

@@ -27,7 +27,8 @@ enum ChunkKind { CK_SKIP = 0, CK_SOFTMAX = 1, CK_ARGMAX = 2 };
 
 struct ChunkRef {
   const void *src;  // first byte of the warp-chunk
-  float2 *dst;      // its partial
+  Part *dst;        // its partial
+  unsigned tag;     // this call's partial tag
   int kind, n, x0;  // n valid elements, x0 = first vocabulary index
   int draft;        // 1: element type DDT, else TDT
   float c;
@@ -68,6 +69,7 @@ __device__ __forceinline__ ChunkRef decode_chunk(const PassParams &P, int k) {
   r.n = min(E, P.V - r.x0);
   r.draft = draft;
   r.dst = P.part + ((size_t)b * P.rows + row) * P.cMax + ci;
+  r.tag = P.part_tag;
   r.c = 0.f;
   if (MODE == MODE_CHAIN || MODE == MODE_DRAFT) {
     const float T = __ldg(P.temps + b);
@@ -212,7 +214,7 @@ __device__ __forceinline__ void chunk_reduce(const ChunkRef &r, const uint4 (&bu
     idx = warp_min_int(idx);
     out = make_float2(m, __int_as_float(idx == 0x7fffffff ? idx : r.x0 + idx));
   }
-  if (lane == 0) *r.dst = out;
+  if (lane == 0) part_store(r.dst, out.x, out.y, r.tag);
 }
 
 template <int MODE, int TDT, int DDT, bool PROBS>
