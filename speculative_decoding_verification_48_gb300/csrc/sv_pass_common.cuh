@@ -106,10 +106,12 @@ struct PassParams {
 };
 
 // Workspace: a header of kPassHeaderBytes (claim counters, error, ready and
-// stamp words), done[B], partials, residual chunk sums.  No initialisation
-// is needed: each call's decide kernel leaves the counters zeroed and
-// stamps them valid, and a stats kernel that finds no valid stamp (a fresh
-// or overwritten workspace) zeroes them itself before any claim.
+// stamp words), done[B], tagged partials, residual chunk sums.  The header
+// is zeroed once by the caller; after that each call's decide kernel leaves
+// the counters zeroed and stamps them valid, and a stats kernel that finds
+// no valid stamp zeroes them itself before any claim.  Nothing after the
+// header needs initialisation: done[] is zeroed by the stats kernel and
+// partials carry their call's tag.
 struct PassLayout {
   size_t claim, err, ready, stamp, done, part, resid, total;
   int cT, cD, cMax, cR;
