@@ -102,16 +102,24 @@ def measured_peak():
     return 6800.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed, so
+    that the hash below changes with the code, not with its comments."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha() -> str:
-    """Hash of the sources the timed chain kernels compile from: the bf16
+    """Hash of the code the timed chain kernels compile from: the bf16
     translation unit, the host launch code and every header it includes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_48_gb300", "csrc")
     files = sorted(f for f in os.listdir(csrc) if f.endswith((".cuh", ".h")))
     files += ["sv_api.cu", "sv_chain_bf16.cu"]
     for f in files:
-        h.update(open(os.path.join(csrc, f), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "spec_verify.h"), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
+    h.update(_code_only(open(os.path.join(ROOT, "include", "spec_verify.h")).read()).encode())
     return h.hexdigest()[:16]
 
 
