@@ -20,6 +20,9 @@ struct DecideSmem {
   float rowM[kMaxRows], rowZ[kMaxRows];
   int rowI[kMaxRows];
   int j, status, last;
+  float tot[kPassWarps];  // the rescan: each warp's share of the crossing chunk's mass
+  int lastp[kPassWarps];  // ... and its last index of positive mass (-1: none)
+  int k;                  // the drawn token
   // per warp: the p and q halves of one residual chunk, copied in by cp.async
   alignas(16) unsigned char stage[kPassWarps][2 * kResidBytes];
 };
@@ -73,8 +76,8 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   int x = 0;
   bool tok_ok = false;
   float lp = 0.f, lq = 0.f, qp = 0.f, ui = 0.f;
-  // the categorical draw, used by warp 0 of whichever CTA draws the token
-  const float ug = (warp == 0 && !badT && !greedy) ? __ldg(P.unif + (size_t)b * G1 + g) : 0.f;
+  // the categorical draw, used by every warp of whichever CTA draws the token
+  const float ug = (!badT && !greedy) ? __ldg(P.unif + (size_t)b * G1 + g) : 0.f;
   if (act) {
     x = __ldg(P.draft_tokens + (size_t)b * g + i);
     tok_ok = x >= 0 && x < V;
@@ -324,30 +327,79 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     sm.last = (prev == (unsigned)P.H - 1u);
   }
   __syncthreads();
-  if (!sm.last || warp != 0) return;
-  // 5. the last CTA: crossing chunk of u * R, then a rescan of that chunk
+  if (!sm.last) return;
+  // 5. the last CTA.  Every warp locates the crossing chunk of u * R from
+  // the same chunk sums; the chunk is rescanned by all eight warps, each
+  // over its eighth, and a prefix over the eight shares picks the warp that
+  // holds the crossing.  Warp 0, whose lanes hold the draft tokens, writes
+  // the row's outputs.
   const float u = ug;
   float R = 0.f, base = 0.f;
   const int t = warp_chunk_cross(P.cR, [&](int k) { return __ldcg(rs + k); }, u, R, base);
-  if (isnan(R) || isinf(R)) {
-    pass_error_row(P, b, SV_ROW_NONFINITE, G1, ot, nullptr);
+  if (isnan(R) || isinf(R) || !(R > 0.f)) {
+    if (warp != 0) return;
+    if (!(R > 0.f) && !isnan(R)) {
+      // no residual mass (p_j == q_j up to rounding): draw from p_j
+      const int k = warp_sample_softmax_row<TDT>(prow, pb + (size_t)j * P.cMax, P.cT, V, Mp, c, u);
+      for (int s = lane; s < G1; s += 32)
+        ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
+      if (lane == 0) {
+        P.out_nacc[b] = j;
+        if (P.out_status) P.out_status[b] = 0;
+        if (P.out_diag) P.out_diag[((size_t)b * g + j) * 4 + 3] = R;
+      }
+    } else {
+      pass_error_row(P, b, SV_ROW_NONFINITE, G1, ot, nullptr);
+    }
     return;
   }
-  int k;
-  if (!(R > 0.f)) {
-    // no residual mass (p_j == q_j up to rounding): draw from p_j
-    k = warp_sample_softmax_row<TDT>(prow, pb + (size_t)j * P.cMax, P.cT, V, Mp, c, u);
-  } else {
-    const float target = u * R;
-    const int x0 = t * PC::kElems;
-    const int n = min(PC::kElems, V - x0);
-    float a[PC::kPer], qv[PC::kPer];
-    lane_consecutive_load<TDT, PC::kPer>(prow + x0, n, -CUDART_INF_F, a);
-    lane_consecutive_load<DDT, PC::kPer>(qrow + x0, n, PROBS ? 0.f : -CUDART_INF_F, qv);
+  const float target = u * R;
+  constexpr int SUB = PC::kElems / kPassWarps, SPER = SUB / 32;
+  static_assert(SPER % 2 == 0, "pairs of elements per lane");
+  const int xs = t * PC::kElems + warp * SUB;
+  const int ns = min(SUB, V - xs);  // at most 0 past the row's end: all padding
+  float a[SPER], qv[SPER];
+  lane_consecutive_load<TDT, SPER>(prow + xs, ns, -CUDART_INF_F, a);
+  lane_consecutive_load<DDT, SPER>(qrow + xs, ns, PROBS ? 0.f : -CUDART_INF_F, qv);
+  float ls = 0.f;
+  int lpos = -1;
 #pragma unroll
-    for (int e = 0; e < PC::kPer; ++e) a[e] = resid_term<PROBS>(a[e], qv[e], rk);
-    k = x0 + warp_rescan<PC::kPer>(a, base, target);
+  for (int e = 0; e < SPER; e += 2) {
+    const float2 r = resid_pair<PROBS>(a[e], a[e + 1], qv[e], qv[e + 1], rk);
+    a[e] = r.x;
+    a[e + 1] = r.y;
   }
+#pragma unroll
+  for (int e = 0; e < SPER; ++e) {
+    ls += a[e];
+    if (a[e] > 0.f) lpos = lane * SPER + e;
+  }
+  const float wt = warp_sum(ls);
+  const int wl = warp_max_int(lpos);
+  if (lane == 0) {
+    sm.tot[warp] = wt;
+    sm.lastp[warp] = wl >= 0 ? xs + wl : -1;
+  }
+  __syncthreads();
+  float bw = base;
+  int hw = -1;
+  for (int w = 0; w < kPassWarps && hw < 0; ++w) {
+    if (bw + sm.tot[w] > target) hw = w;
+    else bw += sm.tot[w];
+  }
+  if (warp == hw) {
+    const int kl = warp_rescan<SPER>(a, bw, target);
+    if (lane == 0) sm.k = xs + kl;
+  } else if (hw < 0 && warp == 0 && lane == 0) {
+    // rounding left no crossing: the last element of positive mass
+    int kk = t * PC::kElems;
+    for (int w = 0; w < kPassWarps; ++w)
+      if (sm.lastp[w] >= 0) kk = sm.lastp[w];
+    sm.k = kk;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const int k = sm.k;
   for (int s = lane; s < G1; s += 32)
     ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
   if (lane == 0) {
