@@ -311,6 +311,35 @@ def other_workloads(sv, dev, stream, peak):
         out[case.name] = {"us_per_call": ms * 1e3, "positions_per_s": case.B * case.gamma / (ms * 1e-3),
                           "GBps": nbytes / (ms * 1e-3) / 1e9, "frac_of_peak": nbytes / (ms * 1e-3) / 1e9 / peak,
                           "algorithmic_bytes": nbytes, "l2": "flushed before each call (256 MB read)"}
+        if name in ("c2", "c1"):
+            # the same single-round call, 100 times in one CUDA graph: the
+            # device time per call without host launch overhead
+            label = case.name + "_graph100"
+            try:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    for _ in range(100):
+                        call()
+                gt = []
+                # a replay runs on the current stream: make that the timed one
+                with torch.cuda.stream(stream):
+                    graph.replay()
+                    torch.cuda.synchronize()
+                    for _ in range(20):
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        graph.replay()
+                        b.record(stream)
+                        b.synchronize()
+                        gt.append(a.elapsed_time(b) / 100)
+                gms = float(np.median(gt))
+                out[label] = {"us_per_call": gms * 1e3,
+                              "positions_per_s": case.B * case.gamma / (gms * 1e-3),
+                              "l2": "inputs L2-resident (100 calls back to back per replay)"}
+                del graph
+            except Exception as e:  # report, never break the bench line
+                out[label] = {"error": repr(e)[:200]}
     # C1 and C2 as batches of independent rounds in one call each (the
     # throughput a batched decode loop sees); C1's batch fits in L2 and is
     # flushed before each call, C2's 1024-round batch (720 MB) is not

@@ -129,8 +129,15 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   // Merging as partials arrive pays off when the stats work is many times
   // what its resident warps hold: the decide CTAs then only become resident
   // in the stats kernel's tail.  On a small call they would be resident
-  // from the start and poll through the whole stats kernel.
-  S.poll = total >= 16LL * grid * kPassWarps;
+  // from the start and poll through the whole stats kernel.  A call captured
+  // into a CUDA graph never polls: every replay carries the tag fixed at
+  // capture, so an earlier replay's partials would look like its own.
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) {
+    (void)cudaGetLastError();
+    capture = cudaStreamCaptureStatusActive;
+  }
+  S.poll = capture == cudaStreamCaptureStatusNone && total >= 16LL * grid * kPassWarps;
   // Both kernels are programmatic dependents of the work before them: the
   // stats kernel of whatever the stream ran last (it waits on the device
   // before touching the workspace), the decide kernel of the stats kernel.
