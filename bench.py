@@ -372,6 +372,26 @@ def other_workloads(sv, dev, stream, peak):
                       "l2": "flushed before each call (256 MB read)" if flush_each
                             else "inputs larger than L2, back-to-back calls"}
         del call
+    # rows that do not start on 16-byte boundaries take the register-tile
+    # kernels: the C3 shape with V = 128257 (bf16 rows of 256514 bytes)
+    try:
+        ucase = W.make_chain("c3_unaligned_B64_g7_V128257_bf16", 1003, 64, 7, 128257, "bf16",
+                             target="zipf", draft_sigma=(0.3, 2.0),
+                             temperature=W._c3_temperature)
+        ucall = ChainCall(sv, ucase, dev, stream)
+        ucall()
+        torch.cuda.synchronize()
+        ubytes = W.chain_algorithmic_bytes(ucase, ucall.out[1].cpu().numpy())
+        _, ums, _ = time_calls(ucall, 200, 10, stream, per_call_events=False)
+        out[ucase.name] = {"us_per_call": ums * 1e3,
+                           "positions_per_s": ucase.B * ucase.gamma / (ums * 1e-3),
+                           "GBps": ubytes / (ums * 1e-3) / 1e9,
+                           "frac_of_peak": ubytes / (ums * 1e-3) / 1e9 / peak,
+                           "algorithmic_bytes": ubytes, "path": "register-tile kernels",
+                           "l2": "inputs larger than L2, back-to-back calls"}
+        del ucall
+    except Exception as e:  # report, never break the bench line
+        out["c3_unaligned_B64_g7_V128257_bf16"] = {"error": repr(e)[:200]}
     # draft-side draws (the draft step before verification): 1024 rows of
     # the 128K vocabulary, back to back (262 MB > L2)
     dcase = W.make_draft("draft_sample_B1024_V128256_bf16", 1006, 1024, 128256, "bf16",
