@@ -39,6 +39,8 @@
  *    (programmatic dependent launch) of the work before them in `stream`:
  *    the first kernel waits on the device for that work to complete before
  *    it touches the workspace, so stream order is kept.
+ *  - Calls may be captured into a CUDA graph.  Each replay verifies the
+ *    inputs found in the captured buffers at replay time.
  *  - Row alignment is the caller's job: target row i scores draft i (the
  *    distribution conditioned on the context and drafts 0..i-1); row gamma is
  *    the bonus row.
