@@ -1,18 +1,24 @@
 """Comparison of library outputs with the float64 oracle (test infrastructure).
 
 Greedy and tree outputs must be bit-exact.  A stochastic row may differ
-only where a floating-point decision is within ``eps`` (1e-5) of its
-boundary:
+only where the one floating-point decision that separates the two results
+lies within ``eps`` (1e-5) of its boundary:
 
-  * an accept test at a position both sides reached, with
-    |u_i - p_i(x_i)/q_i(x_i)| < eps (oracle's float64 ratio), or
-  * the categorical draw at the same rejected/bonus position j, where the
-    library's token k' would be the oracle's choice for a uniform within eps
-    of u, i.e. dist(u, [C(k'-1)/R, C(k')/R)) < eps on the oracle's CDF.
+  * the accept test at the first position where the two sides disagree
+    (one accepted, the other rejected), i = min(j_lib, j_oracle) < gamma,
+    with |u_i - p_i(x_i)/q_i(x_i)| < eps (the oracle's float64 ratio); the
+    draft tokens before i must agree;
+  * with the same first rejection j on both sides, the categorical draw at
+    slot j: the library's token k' must be the oracle's choice for some
+    uniform within eps of u_gamma, i.e. dist(u, [C(k'-1)/R, C(k')/R)) < eps
+    on the oracle's CDF; the drafts before j and the -1 padding after j
+    must agree.
 
 Such rows are counted as boundary cases and reported; any other difference
 is a failure.  Diagnostic probabilities are compared within ``prob_tol``
-(1e-4 for bf16/fp16 logits, 1e-5 for fp32).
+(1e-4 for bf16/fp16 logits, 1e-5 for fp32), the residual mass of a rejected
+row only where both sides rejected at the same position.  Greedy rows carry
+zero diagnostics on both sides.
 """
 
 from __future__ import annotations
@@ -26,6 +32,22 @@ EPS = 1e-5
 
 def prob_tolerance(dtype_name: str) -> float:
     return 1e-5 if dtype_name in ("f32", "float32") else 1e-4
+
+
+def _cdf_distance(args64, b, k, uu):
+    """Distance of the uniform ``uu`` from the oracle's CDF interval of token
+    ``k`` in the distribution row ``b`` drew its last token from."""
+    tl, dr, probs, xt, T, u = args64
+    one = verify_chain(tl[b:b + 1], dr[b:b + 1], probs, xt[b:b + 1], T[b:b + 1],
+                       u[b:b + 1], keep_cdf=True)
+    cdf = one["cdf"][0]
+    if not 0 <= k < cdf.size:
+        return np.inf
+    lo = 0.0 if k == 0 else cdf[k - 1]
+    hi = cdf[k]
+    if np.isnan(lo) or np.isnan(hi):
+        return np.inf
+    return 0.0 if lo <= uu < hi else min(abs(uu - lo), abs(uu - hi))
 
 
 def compare_chain(args64, ref, tokens, nacc, status, diag=None, prob_tol=1e-4, eps=EPS):
@@ -51,42 +73,49 @@ def compare_chain(args64, ref, tokens, nacc, status, diag=None, prob_tol=1e-4, e
             else:
                 exact += 1
             continue
-        same = nacc[b] == ref["num_accepted"][b] and np.array_equal(tokens[b], ref["tokens"][b])
-        if not ref["greedy"][b] and diag is not None:
+        jg, jr = int(nacc[b]), int(ref["num_accepted"][b])
+        same = jg == jr and np.array_equal(tokens[b], ref["tokens"][b])
+        if diag is not None:
             d = np.asarray(diag[b], np.float64)
-            err = np.max(np.abs(d[:, :3] - ref["diag"][b, :, :3]))
-            err = max(err, float(np.max(np.abs(d[:, 3] - ref["diag"][b, :, 3]))) if same else err)
-            diag_err = max(diag_err, float(err))
+            cols = 4 if jg == jr else 3
+            err = float(np.max(np.abs(d[:, :cols] - ref["diag"][b, :, :cols]), initial=0.0))
+            if np.isnan(d[:, :cols]).any():
+                err = np.inf
+            diag_err = max(diag_err, err)
             if err > prob_tol:
-                failures.append((b, "diag", float(err)))
+                failures.append((b, "diag", err))
+                continue
         if same:
             exact += 1
             continue
         if ref["greedy"][b]:
             failures.append((b, "greedy mismatch", tokens[b].tolist(), ref["tokens"][b].tolist()))
             continue
-        jg, jr = int(nacc[b]), int(ref["num_accepted"][b])
-        lim = min(jg, jr)
-        near = [i for i in range(min(lim + 1, g))
-                if abs(u[b, i] - ref["ratio"][b, i]) < eps]
-        if near:
-            boundary.append((b, "accept", near))
+        if not (0 <= jg <= g):
+            failures.append((b, "num_accepted out of range", jg))
             continue
-        if jg == jr and np.array_equal(tokens[b, :jg], ref["tokens"][b, :jr]):
-            one = verify_chain(tl[b:b + 1], dr[b:b + 1], probs, xt[b:b + 1], T[b:b + 1],
-                               u[b:b + 1], keep_cdf=True)
-            cdf = one["cdf"][0]
-            k = int(tokens[b, jg])
-            if 0 <= k < cdf.size:
-                lo = 0.0 if k == 0 else cdf[k - 1]
-                hi = cdf[k]
-                uu = u[b, g]
-                dist = 0.0 if lo <= uu < hi else min(abs(uu - lo), abs(uu - hi))
-                if dist < eps:
-                    boundary.append((b, "sample", k, int(ref["tokens"][b, jr]), dist))
-                    continue
-        failures.append((b, "stochastic mismatch", tokens[b].tolist(),
-                         ref["tokens"][b].tolist()))
+        if jg != jr:
+            # the first position whose accept decision differs
+            i = min(jg, jr)
+            if (np.array_equal(tokens[b, :i], ref["tokens"][b, :i])
+                    and abs(u[b, i] - ref["ratio"][b, i]) < eps):
+                boundary.append((b, "accept", i))
+                continue
+            failures.append((b, "first rejection", jg, jr, tokens[b].tolist(),
+                             ref["tokens"][b].tolist()))
+            continue
+        j = jg
+        if (not np.array_equal(tokens[b, :j], ref["tokens"][b, :j])
+                or np.any(tokens[b, j + 1:] != -1)):
+            failures.append((b, "accepted drafts or padding", tokens[b].tolist(),
+                             ref["tokens"][b].tolist()))
+            continue
+        k = int(tokens[b, j])
+        dist = _cdf_distance(args64, b, k, u[b, g])
+        if dist < eps:
+            boundary.append((b, "sample", k, int(ref["tokens"][b, j]), float(dist)))
+            continue
+        failures.append((b, "draw", k, int(ref["tokens"][b, j]), float(dist)))
     return dict(rows=B, exact=exact, boundary=boundary, failures=failures,
                 diag_max_err=diag_err)
 
