@@ -191,32 +191,59 @@ def make_chain(name: str, seed: int, B: int, gamma: int, V: int, dtype: str = "b
 # The five workloads
 # ---------------------------------------------------------------------------
 
-def c1_chain_fp32_v1000(rounds: int = 256, seed: int = 1001) -> ChainCase:
-    return make_chain("c1_chain_B1x256rounds_g4_V1000_f32", seed, rounds, 4, 1000, "f32",
-                      target="normal", target_sigma=2.0, draft_sigma=(0.5, 0.5),
-                      temperature=1.0)
+def c1_spec(rounds: int = 256, seed: int = 1001) -> dict:
+    """Keyword arguments of ``make_chain`` for C1 (any subset of its rows can
+    be regenerated with ``make_chain(**{**spec, "B": n, "row0": r0})``)."""
+    return dict(name=f"c1_chain_B1x{rounds}rounds_g4_V1000_f32", seed=seed, B=rounds, gamma=4,
+                V=1000, dtype="f32", target="normal", target_sigma=2.0, draft_sigma=(0.5, 0.5),
+                temperature=1.0)
 
 
-def c2_chain_bf16_v32000(T: float, rounds: int = 4096, seed: int = 1002) -> ChainCase:
-    return make_chain(f"c2_chain_B1x{rounds}rounds_g5_V32000_bf16_T{T}", seed, rounds, 5, 32000,
-                      "bf16", target="zipf", draft_sigma=(1.0, 1.0), temperature=float(T))
+def c2_spec(T: float, rounds: int = 4096, seed: int = 1002) -> dict:
+    return dict(name=f"c2_chain_B1x{rounds}rounds_g5_V32000_bf16_T{T}", seed=seed, B=rounds,
+                gamma=5, V=32000, dtype="bf16", target="zipf", draft_sigma=(1.0, 1.0),
+                temperature=float(T))
 
 
 def _c3_temperature(b: int, v: float) -> float:
     return 0.0 if b % 8 == 0 else 1.2 * v
 
 
+def c3_spec(B: int = 64, gamma: int = 7, V: int = 128256, seed: int = 1003) -> dict:
+    return dict(name=f"c3_chain_B{B}_g{gamma}_V{V}_bf16", seed=seed, B=B, gamma=gamma, V=V,
+                dtype="bf16", target="zipf", draft_sigma=(0.3, 2.0), temperature=_c3_temperature)
+
+
+def c5_spec(B: int = 256, gamma: int = 4, V: int = 256000, seed: int = 1005) -> dict:
+    return dict(name=f"c5_chain_B{B}_g{gamma}_V{V}_bf16_f32probs", seed=seed, B=B, gamma=gamma,
+                V=V, dtype="bf16", target="zipf", draft_sigma=(0.7, 0.7), temperature=0.8,
+                draft_probs=True, draft_probs_T=1.0, force_accept_every=16)
+
+
+def c1_chain_fp32_v1000(rounds: int = 256, seed: int = 1001) -> ChainCase:
+    return make_chain(**c1_spec(rounds, seed))
+
+
+def c2_chain_bf16_v32000(T: float, rounds: int = 4096, seed: int = 1002) -> ChainCase:
+    return make_chain(**c2_spec(T, rounds, seed))
+
+
 def c3_chain_bf16_v128256(B: int = 64, gamma: int = 7, V: int = 128256,
                           seed: int = 1003) -> ChainCase:
-    return make_chain(f"c3_chain_B{B}_g{gamma}_V{V}_bf16", seed, B, gamma, V, "bf16",
-                      target="zipf", draft_sigma=(0.3, 2.0), temperature=_c3_temperature)
+    return make_chain(**c3_spec(B, gamma, V, seed))
 
 
 def c5_chain_bf16_probs_v256000(B: int = 256, gamma: int = 4, V: int = 256000,
                                 seed: int = 1005) -> ChainCase:
-    return make_chain(f"c5_chain_B{B}_g{gamma}_V{V}_bf16_f32probs", seed, B, gamma, V, "bf16",
-                      target="zipf", draft_sigma=(0.7, 0.7), temperature=0.8,
-                      draft_probs=True, draft_probs_T=1.0, force_accept_every=16)
+    return make_chain(**c5_spec(B, gamma, V, seed))
+
+
+def concat_chain(parts: Sequence[ChainCase], name: Optional[str] = None) -> ChainCase:
+    """One case holding the rows of ``parts`` in order."""
+    cat = lambda f: torch.cat([getattr(c, f) for c in parts])  # noqa: E731
+    return ChainCase(name or parts[0].name, cat("target"), cat("draft"), parts[0].draft_is_probs,
+                     cat("draft_tokens"), cat("temperatures"), cat("uniforms"),
+                     dict(parts[0].meta))
 
 
 def make_tree(name: str, seed: int, B: int = 16, N: int = 64, V: int = 32000,

@@ -14,6 +14,7 @@ from scipy import special, stats
 
 import oracle
 from oracle.compare import compare_chain, prob_tolerance
+import chunked_oracle as CO
 from speculative_decoding_verification_48_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -83,10 +84,71 @@ def test_c1_chain_fp32_v1000(sv):
     assert cmp["exact"] + len(cmp["boundary"]) == 256
 
 
+@pytest.fixture(scope="module")
+def pool():
+    p = CO.spawn_pool()
+    yield p
+    p.close()
+    p.join()
+
+
+def check_full(sv, pool, spec, gen_chunk, cmp_chunk, tol):
+    """All rows of a workload through one library call, compared with the
+    oracle chunk by chunk in the pool."""
+    case = CO.generate(pool, spec, gen_chunk)
+    B = case.B
+    outs = run_chain(sv, case)
+    del case
+    cmp = CO.compare(pool, spec, outs, cmp_chunk, tol)
+    assert not cmp["failures"], cmp["failures"][:5]
+    assert len(cmp["boundary"]) <= max(2, int(0.01 * B)), cmp["boundary"]
+    assert cmp["exact"] + len(cmp["boundary"]) == B
+    return cmp, outs
+
+
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
-def test_c2_chain_bf16_v32000(sv, T):
-    # the first 512 of the 4096 rounds (rows are generated independently)
-    check_chain(sv, W.c2_chain_bf16_v32000(T, rounds=512))
+def test_c2_chain_bf16_v32000_all_rounds(sv, pool, T):
+    """C2 in full: all 4096 rounds at each temperature in one batched call."""
+    cmp, _ = check_full(sv, pool, W.c2_spec(T), 256, 128, 1e-4)
+    if T == 0.0:
+        assert cmp["greedy"].all()
+    assert len(set(cmp["num_accepted"].tolist())) >= 3
+
+
+def _single_rounds(sv, case, rounds):
+    """One library call per round (B = 1), the call shape the bench times."""
+    args = [t.to(DEV) for t in (case.target, case.draft, case.draft_tokens, case.temperatures,
+                                case.uniforms)]
+    ws = torch.zeros(sv.spec_verify_workspace_bytes(1, 2 * case.gamma + 1, case.V),
+                     dtype=torch.uint8, device=DEV)
+    outs = []
+    for r in rounds:
+        o = sv.spec_verify_chain(*(a[r:r + 1] for a in args), draft_is_probs=case.draft_is_probs,
+                                 workspace=ws)
+        outs.append([t.clone() for t in o])
+    torch.cuda.synchronize()
+    return [np.concatenate([o[k].cpu().numpy() for o in outs]) for k in range(4)]
+
+
+def test_c1_single_round_calls(sv):
+    """C1's 256 rounds, each as its own B = 1 call on one shared workspace."""
+    case = W.c1_chain_fp32_v1000()
+    toks, nacc, diag, st = _single_rounds(sv, case, range(case.B))
+    args = case.numpy64()
+    cmp = compare_chain(args, oracle.verify_chain(*args), toks, nacc, st, diag, prob_tol=1e-5)
+    assert not cmp["failures"], cmp["failures"][:5]
+    assert cmp["exact"] + len(cmp["boundary"]) == 256 and len(cmp["boundary"]) <= 2
+
+
+@pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
+def test_c2_single_round_calls(sv, T):
+    """The first 64 of C2's rounds, each as its own B = 1 call."""
+    case = W.c2_chain_bf16_v32000(T, rounds=64)
+    toks, nacc, diag, st = _single_rounds(sv, case, range(case.B))
+    args = case.numpy64()
+    cmp = compare_chain(args, oracle.verify_chain(*args), toks, nacc, st, diag, prob_tol=1e-4)
+    assert not cmp["failures"], cmp["failures"][:5]
+    assert len(cmp["boundary"]) <= 2
 
 
 def test_c3_chain_bf16_v128256_full(sv):
@@ -102,12 +164,13 @@ def test_c4_tree_f16_full(sv):
     assert ref["num_accepted"].max() >= 3
 
 
-def test_c5_chain_probs_full_sampled_rows(sv):
-    case = W.c5_chain_bf16_probs_v256000()
-    rows = sorted(set(range(0, 256, 16)) | set(range(1, 256, 9)))
-    cmp, ref, out = check_chain(sv, case, rows=rows)
-    forced = [i for i, r in enumerate(rows) if r % 16 == 0]
-    assert np.all(ref["num_accepted"][forced] == 4)
+def test_c5_chain_probs_all_rows(sv, pool):
+    """C5 in full: all 256 rows in one call (bf16 target, fp32 draft
+    probabilities, forced all-accept rows drawing the bonus token)."""
+    cmp, outs = check_full(sv, pool, W.c5_spec(), 16, 8, 1e-4)
+    forced = np.arange(256) % 16 == 0
+    assert np.all(cmp["num_accepted"][forced] == 4)
+    assert (cmp["num_accepted"] == 4).sum() > forced.sum()   # natural all-accepts too
 
 
 # ---------------------------------------------------------------------------
