@@ -58,8 +58,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["c3", "c5", "c2", "c1", "c4"], default="c3",
-                    help="c4 (token trees: mask, greedy walk, KV compaction) is accepted in --ncu mode only")
+    ap.add_argument("--workload", choices=["c3", "c5", "c2", "c1", "c4", "draft"], default="c3",
+                    help="c4 (token trees: mask, greedy walk, KV compaction) and draft (the "
+                         "draft-side sampler, 1024 rows x 128256 bf16) are accepted in --ncu "
+                         "mode only")
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -488,17 +490,41 @@ def other_workloads(sv, dev, stream, peak):
     return out
 
 
+def host_cpu():
+    """The host's logical CPU count and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"^Model name:\s*(.+)$", out, flags=re.M)
+        model = m.group(1).strip() if m else None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model and os.path.exists("/proc/cpuinfo"):
+        txt = open("/proc/cpuinfo").read()
+        m = re.search(r"^(model name|Hardware|CPU part)\s*:\s*(.+)$", txt, flags=re.M)
+        model = m.group(2).strip() if m else None
+    return os.cpu_count(), model
+
+
 def cpu_baseline(case, seconds):
-    """The float64 oracle as it stands, single process: whole passes over the
-    workload's batch rows, repeated until about `seconds` of CPU work."""
+    """The float64 oracle as it stands, single process pinned to one core:
+    whole passes over the workload's batch rows, repeated until about
+    `seconds` of CPU work."""
     import oracle
     args = case.numpy64()
-    passes, dt = 0, 0.0
-    while dt < seconds or passes == 0:
-        t = time.perf_counter()
-        oracle.verify_chain(*args)
-        dt += time.perf_counter() - t
-        passes += 1
+    aff = os.sched_getaffinity(0) if hasattr(os, "sched_getaffinity") else None
+    if aff:
+        os.sched_setaffinity(0, {min(aff)})
+    try:
+        passes, dt = 0, 0.0
+        while dt < seconds or passes == 0:
+            t = time.perf_counter()
+            oracle.verify_chain(*args)
+            dt += time.perf_counter() - t
+            passes += 1
+    finally:
+        if aff:
+            os.sched_setaffinity(0, aff)
     return passes * case.B * case.gamma / dt, dt, passes
 
 
@@ -599,6 +625,15 @@ def main():
                                     nacc.repeat(32).contiguous(), stream=stream)
         torch.cuda.synchronize()
         return
+    if a.ncu and a.workload == "draft":
+        # the draft-side sampler: 1024 rows of the 128K vocabulary (262 MB)
+        dcase = W.make_draft("draft_sample_B1024_V128256_bf16", 1006, 1024, 128256, "bf16",
+                             temperature=lambda b, v: 0.0 if b % 8 == 0 else 0.2 + v)
+        dl, dT, du = (t.to(dev) for t in (dcase.logits, dcase.temperatures, dcase.uniforms))
+        for _ in range(1 + a.warmup + a.steps):
+            sv.spec_draft_sample(dl, dT, du, stream=stream)
+        torch.cuda.synchronize()
+        return
     case = make_workload(a.workload, row0=rank_row0(rank))
     call = ChainCall(sv, case, dev, stream)
     call()
@@ -656,10 +691,36 @@ def main():
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1:
+        # the same call with L2 flushed before each call (a 256 MB read on the
+        # call's stream), beside the back-to-back figure above
+        flush = torch.ones(128 * 1024 * 1024, dtype=torch.float16, device=dev)
+        ft = []
+        for _ in range(200):
+            with torch.cuda.stream(stream):
+                flush.sum()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            ft.append(e0.elapsed_time(e1))
+        del flush
+        fms = float(np.median(ft))
+        line["l2_flushed"] = {"us_per_call": fms * 1e3,
+                              "positions_per_s": positions / (fms * 1e-3),
+                              "GBps": alg_bytes / (fms * 1e-3) / 1e9,
+                              "frac_of_peak": alg_bytes / (fms * 1e-3) / 1e9 / peak,
+                              "calls": len(ft),
+                              "how": "median of single calls, each after a 256 MB read on "
+                                     "the call's stream"}
         v, dt, passes = cpu_baseline(case, a.cpu_seconds)
+        nproc, model = host_cpu()
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "host_nproc": nproc, "host_cpu": model,
                                 "sample": f"{passes} passes over the {case.B} batch rows of "
-                                          f"{case.name} ({dt:.1f} s, single process)"}
+                                          f"{case.name} ({dt:.1f} s, single process pinned "
+                                          f"to one core)"}
         if not a.quick:
             line["other_workloads"] = other_workloads(sv, dev, stream, peak)
     if rank == 0:

@@ -26,15 +26,17 @@
  *    enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *  - `workspace` is caller-owned device memory of at least
  *    spec_verify_workspace_bytes(...) bytes, 16-byte aligned.  Its first
- *    4096 bytes hold library state between calls (work-claim counters, left
- *    zeroed by every call and stamped valid; a call that finds no valid
- *    stamp resets them itself).  Those 4096 bytes must be zero before the
- *    first call on the memory, and again whenever the caller has used that
- *    memory for anything else in between: recycled memory can hold a stale
- *    valid stamp above non-zero counters, which the library cannot tell from
- *    its own state.  The rest of the workspace needs no initialisation.
- *    Calls that may overlap on the GPU need distinct workspaces; calls in
- *    stream order may share one, whatever their shapes.
+ *    4096 bytes hold library state between calls: work-claim counters, left
+ *    zeroed by every call and stamped valid (a call that finds no valid
+ *    stamp resets them itself), and a call epoch that the kernels advance
+ *    by one per call, CUDA graph replays included.  Those 4096 bytes must
+ *    be zero before the first call on the memory, and again whenever the
+ *    caller has used that memory for anything else in between: recycled
+ *    memory can hold a stale valid stamp above non-zero counters, which the
+ *    library cannot tell from its own state.  The rest of the workspace
+ *    needs no initialisation.  Calls that may overlap on the GPU need
+ *    distinct workspaces; calls in stream order may share one, whatever
+ *    their shapes.
  *  - Each call enqueues its kernels as programmatic dependents
  *    (programmatic dependent launch) of the work before them in `stream`:
  *    the first kernel waits on the device for that work to complete before
@@ -271,6 +273,18 @@ SV_API sv_status spec_tree_kv_compact(void *kv, size_t row_bytes, int B, int S,
 SV_API sv_status spec_verify_wait_selftest(int which, void *scratch, int32_t *out_status,
                                            sv_stream_t stream);
 
+/*
+ * Diagnostics.  Sets the process-wide call counter that numbers the
+ * library's calls and returns its previous value.  The next call gets
+ * number calls + 1.  A call's number tags the partial results its first
+ * kernel hands to its second; only calls numbered below 2^31 let the second
+ * kernel merge tagged partials as they arrive (the tags of those calls are
+ * all distinct), later calls wait for the first kernel to finish.  Tests use
+ * this to reach that limit.  Moving the counter backwards can repeat tags of
+ * earlier calls and is not supported.
+ */
+SV_API unsigned long long spec_verify_set_call_counter(unsigned long long calls);
+
 /* Static description of a status code; never NULL. */
 SV_API const char *spec_verify_status_string(sv_status s);
 
@@ -298,7 +312,11 @@ SV_API const char *spec_verify_status_string(sv_status s);
  *    B=64, gamma=7, V=128256 needs about 2 MB.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.  A failed lookup returns SV_ERR_CUDA.
+ *    before any stream capture.  A failed lookup returns SV_ERR_CUDA.  The
+ *    address is kept for the life of the process and belongs to the
+ *    device's primary context: do not use this function after
+ *    cudaDeviceReset, nor under a context made current through the driver
+ *    API.
  *  - Every call on a device shares the one array.  Calls that may overlap
  *    on the GPU (different streams, or different host threads without
  *    ordering) race on it and give wrong results: keep them in one stream

@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.spec_tree_kv_compact.restype = _INT
             L.spec_verify_wait_selftest.argtypes = [_INT, _VP, _I32P, _VP]
             L.spec_verify_wait_selftest.restype = _INT
+            L.spec_verify_set_call_counter.argtypes = [ctypes.c_ulonglong]
+            L.spec_verify_set_call_counter.restype = ctypes.c_ulonglong
             L.spec_verify_status_string.argtypes = [_INT]
             L.spec_verify_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -93,6 +95,12 @@ def lib() -> ctypes.CDLL:
 
 def spec_verify_status_string(status: int) -> str:
     return lib().spec_verify_status_string(int(status)).decode()
+
+
+def spec_verify_set_call_counter(calls: int) -> int:
+    """Diagnostics: set the library's process-wide call counter; returns the
+    previous value (see spec_verify_set_call_counter in spec_verify.h)."""
+    return int(lib().spec_verify_set_call_counter(int(calls)))
 
 
 def spec_verify_workspace_bytes(B: int, rows_per_batch: int, V: int, dtype: int = SV_BF16) -> int:

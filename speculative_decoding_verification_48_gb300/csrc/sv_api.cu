@@ -65,9 +65,10 @@ static void fill_workspace(KParams &P, void *ws, const Layout &L) {
   P.tiles = L.tiles;
 }
 
+static std::atomic<unsigned long long> g_calls{0};
+
 unsigned long long next_call_id() {
-  static std::atomic<unsigned long long> calls{0};
-  return calls.fetch_add(1, std::memory_order_relaxed) + 1;
+  return g_calls.fetch_add(1, std::memory_order_relaxed) + 1;
 }
 
 }  // namespace sv
@@ -245,6 +246,10 @@ SV_API sv_status spec_draft_sample(const void *logits, sv_dtype dt, const float 
   P.out_status = out_row_status;
   fill_workspace(P, workspace, make_layout(B, 1, V));
   return launch_draft(P, dt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SV_API unsigned long long spec_verify_set_call_counter(unsigned long long calls) {
+  return g_calls.exchange(calls, std::memory_order_relaxed);
 }
 
 SV_API const char *spec_verify_status_string(sv_status s) {

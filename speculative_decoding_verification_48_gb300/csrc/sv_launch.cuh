@@ -10,6 +10,21 @@ namespace sv {
 
 constexpr int kMaxDevices = 64;
 
+// Partials are polled (merged before the dependency wait) only by the first
+// kPollCalls calls of the process: their tags, below, are then all
+// distinct, so a partial left in a workspace by an earlier call never
+// carries a polling call's tag.  Later calls take the dependency wait.
+constexpr unsigned long long kPollCalls = 1ull << 31;
+
+// The 32-bit tag of a call's partials: (2 id + 1) times an odd constant,
+// modulo 2^32.  It is odd, so never the tag of a zeroed word, and distinct
+// for ids below 2^31; the multiplication spreads consecutive ids over the
+// whole range, so small integers left in recycled memory do not resemble
+// early calls' tags.
+inline unsigned partial_tag(unsigned long long call_id) {
+  return (unsigned)((call_id << 1) | 1ull) * 0x9E3779B1u;
+}
+
 // Launches one instantiation with the call's schedule.  The grid is one
 // wave of resident CTAs (SM count x occupancy), capped by the unit count;
 // CTAs pull units from the workspace counter.
@@ -117,8 +132,10 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   S.claim_err = reinterpret_cast<unsigned long long *>(w + L.err);
   S.claim_ready = reinterpret_cast<unsigned long long *>(w + L.ready);
   S.claim_stamp = reinterpret_cast<unsigned long long *>(w + L.stamp);
-  S.call_id = next_call_id();                    // never 0, unique in the process
-  S.part_tag = (unsigned)(S.call_id << 1) | 1u;  // odd: never a zeroed word's
+  S.epoch_base = reinterpret_cast<unsigned long long *>(w + L.epoch_base);
+  S.epoch_cur = reinterpret_cast<unsigned long long *>(w + L.epoch_cur);
+  const unsigned long long call_id = next_call_id();
+  S.part_tag = partial_tag(call_id);
   S.done = reinterpret_cast<unsigned *>(w + L.done);
   S.part = reinterpret_cast<Part *>(w + L.part);
   S.resid = reinterpret_cast<float *>(w + L.resid);
@@ -137,7 +154,8 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
     (void)cudaGetLastError();
     capture = cudaStreamCaptureStatusActive;
   }
-  S.poll = capture == cudaStreamCaptureStatusNone && total >= 16LL * grid * kPassWarps;
+  S.poll = capture == cudaStreamCaptureStatusNone && total >= 16LL * grid * kPassWarps &&
+           call_id < kPollCalls;
   // Both kernels are programmatic dependents of the work before them: the
   // stats kernel of whatever the stream ran last (it waits on the device
   // before touching the workspace), the decide kernel of the stats kernel.
@@ -163,9 +181,11 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, decide, S) != cudaSuccess) {
-    // the claim counters were used and will not be reset: drop their stamp
-    // so the next call on this workspace resets them itself
-    (void)cudaMemsetAsync(S.claim_stamp, 0, sizeof(unsigned long long), stream);
+    // The claim counters were used and will not be reset, and the epoch
+    // will not advance: clear the error, ready and stamp words, so that the
+    // next call on this workspace (which reuses this call's epoch) resets
+    // the counters itself and finds no word left by this call.
+    (void)cudaMemsetAsync(w + L.err, 0, L.stamp + sizeof(unsigned long long) - L.err, stream);
     return SV_ERR_CUDA;
   }
   return SV_OK;

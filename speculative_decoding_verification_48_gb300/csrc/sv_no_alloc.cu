@@ -22,7 +22,10 @@ std::atomic<void *> g_scratch_addr[kMaxDev];
 std::mutex g_setup_mutex;
 
 // Device address of the scratch array on the current device, looked up on
-// the first call made with that device current; nullptr on failure.
+// the first call made with that device current; nullptr on failure.  The
+// address belongs to the device's primary context as it was at that first
+// call: it is not looked up again after cudaDeviceReset, nor for a context
+// the caller made current through the driver API.
 void *scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
@@ -59,9 +62,10 @@ SV_API sv_status spec_verify_chain_no_alloc(const void *target_logits, sv_dtype 
   if (need > (size_t)SV_NO_ALLOC_SCRATCH_BYTES) return SV_ERR_UNSUPPORTED;
   void *scratch = scratch_on_current_device();
   if (scratch == nullptr) return SV_ERR_CUDA;
-  // The regular entry point needs no initialised workspace (every call either
-  // finds the state that the previous call left valid or resets it), so what
-  // an earlier call left in the array does not matter.
+  // The array starts zeroed (a static device array) and only these calls
+  // write it.  Each call leaves its 4 KB state header valid for the next
+  // one, whatever the shapes, so the regular entry point can run on it
+  // without further initialisation.
   return spec_verify_chain(target_logits, tdt, draft, ddt, draft_is_probs, draft_tokens,
                            temperatures, uniforms, B, gamma, V, out_tokens, out_num_accepted,
                            out_diag, out_row_status, scratch,

@@ -93,27 +93,39 @@ struct PassParams {
   int32_t *out_tokens, *out_nacc, *out_status, *out_path;
   float *out_diag;
   unsigned *claim;   // [kClaimStripes * kClaimStride] stats-kernel claim counters
-  unsigned long long *claim_err;    // == call_id: this call's stats kernel hit a bound
-  unsigned long long *claim_ready;  // == call_id: this call's stats kernel zeroed the counters
+  unsigned long long *claim_err;    // == this call's epoch: its stats kernel hit a bound
+  unsigned long long *claim_ready;  // == this call's epoch: its stats kernel zeroed the counters
   unsigned long long *claim_stamp;  // == kStampValid: the counters are zero (left so by the
                                     // previous call's decide kernel)
-  unsigned long long call_id;       // unique per call, never 0
+  unsigned long long *epoch_base;   // epoch of the last call that completed on this workspace
+  unsigned long long *epoch_cur;    // epoch of the running call (epoch_base + 1)
   unsigned *done;    // [B] residual-sweep arrivals
   Part *part;        // [B][rows][cMax] warp-chunk partials
-  unsigned part_tag; // odd, from call_id: marks this call's partials
+  unsigned part_tag; // odd, from the host's call id: marks this call's partials
   int poll;          // 1: the decide kernel merges as partials arrive (large calls)
   float *resid;      // [B][cR] residual mass per chunk of the rejected row pair
 };
 
-// Workspace: a header of kPassHeaderBytes (claim counters, error, ready and
-// stamp words), done[B], tagged partials, residual chunk sums.  The header
-// is zeroed once by the caller; after that each call's decide kernel leaves
-// the counters zeroed and stamps them valid, and a stats kernel that finds
-// no valid stamp zeroes them itself before any claim.  Nothing after the
-// header needs initialisation: done[] is zeroed by the stats kernel and
-// partials carry their call's tag.
+// Workspace: a header of kPassHeaderBytes (claim counters; error, ready,
+// stamp and epoch words), done[B], tagged partials, residual chunk sums.
+//
+// The header must be zero before the first call on the memory (and after
+// the caller used the memory for anything else).  From then on every call
+// keeps it valid: each call's decide kernel leaves the counters zeroed,
+// records the call's epoch and stamps the counters valid, and a stats kernel
+// that finds no valid stamp zeroes the counters itself before any claim.
+//
+// Epochs are counted on the device, one per call on the workspace (CUDA
+// graph replays included): the stats kernel takes E = epoch_base + 1 after
+// its dependency wait and publishes it in epoch_cur; the decide kernel reads
+// epoch_cur after its own wait, and its CTA 0 sets epoch_base = E.  The
+// error and ready words are compared with E, so a value left by an earlier
+// call or replay never matches.
+//
+// Nothing after the header needs initialisation: done[] is zeroed by the
+// stats kernel and partials carry their call's tag.
 struct PassLayout {
-  size_t claim, err, ready, stamp, done, part, resid, total;
+  size_t claim, err, ready, stamp, epoch_base, epoch_cur, done, part, resid, total;
   int cT, cD, cMax, cR;
 };
 
@@ -129,6 +141,8 @@ inline PassLayout make_pass_layout(int B, int rows, int V, int esT, int esD, boo
   L.err = (size_t)kClaimStripes * kClaimStride * 4;
   L.ready = L.err + 128;
   L.stamp = L.ready + 128;
+  L.epoch_base = L.stamp + 128;
+  L.epoch_cur = L.epoch_base + 128;
   size_t off = kPassHeaderBytes;
   L.done = off;  off = align_up(off + (size_t)B * 4, 256);
   L.part = off;  off = align_up(off + (size_t)B * rows * L.cMax * sizeof(Part), 256);

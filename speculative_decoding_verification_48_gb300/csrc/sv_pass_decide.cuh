@@ -119,7 +119,7 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   bool claim_err = false;
   if (!polled) {
     grid_dependency_wait();
-    if (warp == 0) claim_err = __ldcg(P.claim_err) == P.call_id;
+    if (warp == 0) claim_err = __ldcg(P.claim_err) == __ldcg(P.epoch_cur);
   }
   if (badT) {
     if (warp == 0) {
@@ -458,7 +458,7 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
     if (n == 0 ? par != -1 : (par < 0 || par >= n)) flags |= SV_ROW_BAD_TREE;
     if (n > 0 && (tok < 0 || tok >= V)) flags |= SV_ROW_BAD_TOKEN;
   }
-  if (threadIdx.x == 0 && __ldcg(P.claim_err) == P.call_id) flags |= SV_ROW_TIMEOUT;
+  if (threadIdx.x == 0 && __ldcg(P.claim_err) == __ldcg(P.epoch_cur)) flags |= SV_ROW_TIMEOUT;
   if (flags) atomicOr(&sm.flags, flags);
   __syncthreads();
   if (warp != 0) return;
@@ -525,7 +525,7 @@ __device__ void decide_draft_row(const PassParams &P, int b) {
       prob = ex2((Elt<DT>::load1(row + tok) - mz.x) * c) / mz.y;
     }
   }
-  if (__ldcg(P.claim_err) == P.call_id) status = SV_ROW_TIMEOUT;
+  if (__ldcg(P.claim_err) == __ldcg(P.epoch_cur)) status = SV_ROW_TIMEOUT;
   if (lane == 0) {
     P.out_tokens[b] = status ? -1 : tok;
     if (P.out_diag) P.out_diag[b] = status ? 0.f : prob;
@@ -538,9 +538,11 @@ __global__ void __launch_bounds__(kPassThreads, 4) sv_decide_kernel(const PassPa
   const int b = blockIdx.x / P.H, h = blockIdx.x - b * P.H;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     // the stats kernel has finished with its claim counters: leave them
-    // zeroed and stamped valid for the next call on this workspace
+    // zeroed, record this call's epoch and stamp the counters valid for the
+    // next call on this workspace (which reads them after this grid ends)
     grid_dependency_wait();
     for (int s = 0; s < kClaimStripes; ++s) P.claim[s * kClaimStride] = 0u;
+    *P.epoch_base = __ldcg(P.epoch_cur);
     __threadfence();
     st_release_u64(P.claim_stamp, kStampValid);
   }

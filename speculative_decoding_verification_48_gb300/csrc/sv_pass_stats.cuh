@@ -235,18 +235,21 @@ struct Claimer {
   int s;
 };
 
-__device__ __forceinline__ void claim_fail(const PassParams &P) {
-  if (lane_id() == 0) *reinterpret_cast<volatile unsigned long long *>(P.claim_err) = P.call_id;
+// Flags this call (epoch E) as unfinished: its decide kernel then reports
+// SV_ROW_TIMEOUT on every row.
+__device__ __forceinline__ void claim_fail(const PassParams &P, unsigned long long E) {
+  if (lane_id() == 0) *reinterpret_cast<volatile unsigned long long *>(P.claim_err) = E;
 }
 
-// Bounded wait until this call's stats kernel has zeroed the counters (slow
-// path only); false, with the call flagged, if the bound is hit.
-__device__ __forceinline__ bool counters_reset_wait(const PassParams &P) {
+// Bounded wait until this call's stats kernel (epoch E) has zeroed the
+// counters (slow path only); false, with the call flagged, if the bound is
+// hit.
+__device__ __forceinline__ bool counters_reset_wait(const PassParams &P, unsigned long long E) {
   bool ok = true;
   if (lane_id() == 0) {
     ok = false;
     for (long long it = 0; it < kReadySpins; ++it) {
-      if (ld_acquire_u64(P.claim_ready) == P.call_id) {
+      if (ld_acquire_u64(P.claim_ready) == E) {
         ok = true;
         break;
       }
@@ -254,7 +257,7 @@ __device__ __forceinline__ bool counters_reset_wait(const PassParams &P) {
     }
   }
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (!ok) claim_fail(P);
+  if (!ok) claim_fail(P, E);
   return ok;
 }
 
@@ -264,7 +267,8 @@ __device__ __forceinline__ unsigned claim_issue(const PassParams &P, const Claim
   return v;
 }
 
-__device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, unsigned pend) {
+__device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, unsigned pend,
+                                             unsigned long long E) {
   const int lane = lane_id();
   long long k = (long long)__shfl_sync(0xffffffffu, pend, 0) * kClaimStripes + c.s;
   // every probe finds a stripe with chunks left or ends the loop; a claim
@@ -272,7 +276,7 @@ __device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, un
   // practice — if it were, the call is flagged rather than left unfinished
   for (int probe = 0; k >= P.total; ++probe) {
     if (probe == kClaimProbes) {
-      claim_fail(P);
+      claim_fail(P, E);
       return -1;
     }
     unsigned cnt = 0xffffffffu;
@@ -295,6 +299,10 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
   // ran before (typically the previous call's decide kernel): nothing of the
   // workspace is touched before that work has completed.
   grid_dependency_wait();
+  // This call's epoch.  epoch_base is written only by this call's decide
+  // kernel after this grid has completed, so every CTA reads the same value.
+  const unsigned long long E = __ldcg(P.epoch_base) + 1ull;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *P.epoch_cur = E;
   // residual-sweep arrival counters of this call start at zero (the decide
   // kernel reads them only after this grid has completed)
   for (int i = blockIdx.x * kPassThreads + threadIdx.x; i < P.B; i += gridDim.x * kPassThreads)
@@ -307,19 +315,19 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
   if (!stamped && blockIdx.x == 0 && threadIdx.x == 0) {
     for (int s = 0; s < kClaimStripes; ++s) P.claim[s * kClaimStride] = 0u;
     __threadfence();
-    st_release_u64(P.claim_ready, P.call_id);
+    st_release_u64(P.claim_ready, E);
   }
   Claimer cl{(int)((blockIdx.x * kPassWarps + warp_id()) % kClaimStripes)};
-  if (!stamped && !counters_reset_wait(P)) return;
+  if (!stamped && !counters_reset_wait(P, E)) return;
   uint4 b0[kChunkVecs], b1[kChunkVecs];
-  int ka = claim_resolve(P, cl, claim_issue(P, cl));
+  int ka = claim_resolve(P, cl, claim_issue(P, cl), E);
   if (ka >= 0) {
     ChunkRef ra = decode_chunk<MODE, TDT, DDT, PROBS>(P, ka);
     chunk_issue<TDT, DDT>(ra, b0);
     unsigned pend = claim_issue(P, cl);  // the next claim is in flight while a chunk is reduced
     // two chunks per iteration so both buffers have static names
     while (true) {
-      const int kb = claim_resolve(P, cl, pend);
+      const int kb = claim_resolve(P, cl, pend, E);
       ChunkRef rb;
       rb.kind = CK_SKIP;
       if (kb >= 0) {
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
       }
       chunk_process<MODE, TDT, DDT, PROBS>(ra, b0);
       if (kb < 0) break;
-      ka = claim_resolve(P, cl, pend);
+      ka = claim_resolve(P, cl, pend, E);
       if (ka >= 0) {
         ra = decode_chunk<MODE, TDT, DDT, PROBS>(P, ka);
         chunk_issue<TDT, DDT>(ra, b0);

@@ -13,12 +13,12 @@ __global__ void sv_wait_selftest_kernel(int which, unsigned long long *scratch,
   if (threadIdx.x >= 32) return;
   if (which == 0) {
     PassParams P{};
-    P.claim_ready = scratch;  // stays 0, never this call's id
+    P.claim_ready = scratch;  // stays 0, never this call's epoch
     P.claim_err = scratch + 1;
-    P.call_id = 1;
-    const bool ok = counters_reset_wait(P);
+    const unsigned long long E = 1;
+    const bool ok = counters_reset_wait(P, E);
     if (lane_id() == 0) {
-      const bool flagged = __ldcg(scratch + 1) == P.call_id;
+      const bool flagged = __ldcg(scratch + 1) == E;
       *out_status = ok ? SV_ROW_OK : (flagged ? SV_ROW_TIMEOUT : SV_ROW_NONFINITE);
     }
   } else if (threadIdx.x == 0) {

@@ -4,8 +4,8 @@ already reserved the whole GPU, or a decode loop that must not call
 cudaMalloc because it can synchronise the device).  Its scratch memory is a
 fixed 8 MiB array inside the library instead of a caller-provided workspace.
 
-The test calls it through the C ABI twice in a row, with different shapes,
-and checks each result against the regular spec_verify_chain on the same
+The test calls it through the C ABI three times in a row, with different
+shapes, and checks each result against the regular spec_verify_chain on the same
 inputs: the same accepted counts and tokens, and diagnostics within the
 probability tolerance the parity tests use.  It also checks that a shape
 whose workspace would not fit in the array is refused before anything is
@@ -80,7 +80,7 @@ def _check_against_regular(sv, case):
     return o
 
 
-def test_no_alloc_matches_regular_entry_point_twice(sv):
+def test_no_alloc_matches_regular_entry_point_three_calls_in_a_row(sv):
     # first call: batched chain with greedy rows and rejections everywhere
     first = W.make_chain("no_alloc_a", 4101, B=24, gamma=7, V=50000, dtype="bf16",
                          target="zipf", draft_sigma=(0.3, 2.0),
@@ -92,6 +92,14 @@ def test_no_alloc_matches_regular_entry_point_twice(sv):
     second = W.make_chain("no_alloc_b", 4102, B=40, gamma=4, V=20001, dtype="f32",
                           draft_sigma=(0.2, 1.5), temperature=lambda b, v: 0.3 + v)
     _check_against_regular(sv, second)
+    # third call: rows on 16-byte boundaries again, with another batch size
+    # and gamma, and the draft given as fp32 probabilities (forced all-accept
+    # rows draw the bonus token)
+    third = W.make_chain("no_alloc_c", 4103, B=33, gamma=5, V=32000, dtype="bf16",
+                         target="zipf", draft_sigma=(0.7, 0.7), temperature=0.8,
+                         draft_probs=True, force_accept_every=4)
+    o3 = _check_against_regular(sv, third)
+    assert np.all(o3[1][::4] == 5)
 
 
 def test_no_alloc_refuses_shapes_beyond_the_scratch_array(sv):
