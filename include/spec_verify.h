@@ -51,9 +51,10 @@
  *    trees) are reported per row in `out_row_status` (bit mask SV_ROW_*); such
  *    a row gets num_accepted = 0 and every token -1.
  *  - Every pointer must be aligned to its element type (out_diag to 16
- *    bytes); otherwise the call returns SV_ERR_INVALID_ARG.  16-byte vector
- *    loads are used when a row starts on a 16-byte boundary; other rows take
- *    a scalar path.  Any V >= 1 is accepted.
+ *    bytes); otherwise the call returns SV_ERR_INVALID_ARG.  Any V >= 1 and
+ *    any row alignment are accepted.  Rows are streamed on each row's own
+ *    16-byte grid (whole aligned 16-byte blocks); the bytes of a block that
+ *    lie outside the row are masked, never used.
  *  - No function throws; all are thread-safe given distinct workspaces.
  */
 #ifndef SPEC_VERIFY_H_
@@ -201,8 +202,8 @@ SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
  *  out_probs    nullable fp32 [B]: q(token) (0 for greedy and invalid rows).
  *  out_row_status nullable int32 [B]: SV_ROW_* bits.
  *  workspace: spec_verify_workspace_bytes(B, 1, V, dt) bytes.
- *  Rows must start on 16-byte boundaries (16-byte aligned `logits`, V times
- *  the element size a multiple of 16); otherwise SV_ERR_UNSUPPORTED.
+ *  Any V >= 1 and any row alignment (the pointer aligned to its element
+ *  type) are accepted.
  */
 SV_API sv_status spec_draft_sample(const void *logits, sv_dtype dt, const float *temperatures,
                                    const float *uniforms, int B, int V, int32_t *out_tokens,
@@ -262,8 +263,9 @@ SV_API sv_status spec_tree_kv_compact(void *kv, size_t row_bytes, int B, int S,
  * same event as SV_ROW_TIMEOUT in out_row_status).
  *  which        0: the stats kernel's wait for its claim counters to be reset
  *               (a spin bound, about a second);
- *               1: the register-tile kernels' wait for a row's decision flag
- *               (2e9 clock cycles, about a second).
+ *               1: the decide kernel's poll of a row's chunk partials for
+ *               the call's tag (a bound of 512 polling rounds, after which
+ *               the decide kernel waits for the stats kernel instead).
  *  scratch      device memory of at least 64 bytes, 16-byte aligned; the call
  *               zeroes and uses it.
  *  out_status   device int32 [1]: SV_ROW_TIMEOUT when the wait ran out, the
@@ -272,6 +274,16 @@ SV_API sv_status spec_tree_kv_compact(void *kv, size_t row_bytes, int B, int S,
  */
 SV_API sv_status spec_verify_wait_selftest(int which, void *scratch, int32_t *out_status,
                                            sv_stream_t stream);
+
+/*
+ * Diagnostics.  Small calls (chains whose kept row slices fit one cluster of
+ * at most 8 CTAs per batch row, trees of at most 1 MB of node-row slices per
+ * CTA, in one wave) run on the cluster path: one launch, no workspace use.
+ * Every other call runs the two-launch streaming path.  With on != 0 every
+ * call takes the streaming path (tests use this to check both paths on the
+ * same shapes); returns the previous setting.  Process-wide.
+ */
+SV_API int spec_verify_force_stream_path(int on);
 
 /*
  * Diagnostics.  Sets the process-wide call counter that numbers the

@@ -10,6 +10,6 @@ from .binding import (  # noqa: F401
     SV_BF16, SV_F16, SV_F32, SV_ROW_BAD_TEMPERATURE, SV_ROW_BAD_TOKEN, SV_ROW_BAD_TREE,
     SV_ROW_NONFINITE, SV_ROW_OK, SV_ROW_TIMEOUT, SpecVerifyError, lib, library_path,
     spec_draft_sample, spec_tree_kv_compact, spec_tree_mask, spec_verify_chain,
-    spec_verify_chain_greedy, spec_verify_set_call_counter, spec_verify_status_string,
+    spec_verify_chain_greedy, spec_verify_force_stream_path, spec_verify_set_call_counter, spec_verify_status_string,
     spec_verify_tree_greedy, spec_verify_wait_selftest, spec_verify_workspace_bytes,
 )

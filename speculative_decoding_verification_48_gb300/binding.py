@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.spec_tree_kv_compact.restype = _INT
             L.spec_verify_wait_selftest.argtypes = [_INT, _VP, _I32P, _VP]
             L.spec_verify_wait_selftest.restype = _INT
+            L.spec_verify_force_stream_path.argtypes = [_INT]
+            L.spec_verify_force_stream_path.restype = _INT
             L.spec_verify_set_call_counter.argtypes = [ctypes.c_ulonglong]
             L.spec_verify_set_call_counter.restype = ctypes.c_ulonglong
             L.spec_verify_status_string.argtypes = [_INT]
@@ -95,6 +97,13 @@ def lib() -> ctypes.CDLL:
 
 def spec_verify_status_string(status: int) -> str:
     return lib().spec_verify_status_string(int(status)).decode()
+
+
+def spec_verify_force_stream_path(on: bool) -> bool:
+    """Diagnostics: make every call take the two-launch streaming path
+    (on=True) or let small calls take the cluster path (on=False); returns
+    the previous setting (see spec_verify_force_stream_path in spec_verify.h)."""
+    return bool(lib().spec_verify_force_stream_path(int(bool(on))))
 
 
 def spec_verify_set_call_counter(calls: int) -> int:

@@ -2,7 +2,6 @@
 // parameter packing and dispatch.  Every check that can fail happens before
 // the first CUDA call, so an invalid call touches no GPU state.
 #include <atomic>
-#include <cstdlib>
 
 #include "sv_pass_common.cuh"
 
@@ -20,10 +19,9 @@ int sm_count(int device) {
 }
 
 size_t workspace_bytes_any(int B, int rows, int V) {
-  const size_t a = kPassHeaderBytes + make_layout(B, rows, V).total;
-  // fp32 rows give the most warp-chunks
-  const size_t b = make_pass_layout(B, rows, V, 4, 4, true).total;
-  return a > b ? a : b;
+  // fp32 rows off the 16-byte grid give the most warp-chunks and residual
+  // chunks
+  return make_pass_layout(B, rows, V, 4, 4, true, true).total;
 }
 
 static bool valid_dtype(int d) { return d == SV_F32 || d == SV_BF16 || d == SV_F16; }
@@ -35,37 +33,10 @@ static bool aligned_to(const void *p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
 
-// The streaming kernel is used for aligned rows unless SPEC_VERIFY_KERNEL=tile
-// selects the register-tile kernel for every shape (for comparisons).
-static int stream_enabled() {
-  static const int v = [] {
-    const char *e = getenv("SPEC_VERIFY_KERNEL");
-    return (e && e[0] == 't') ? 0 : 1;
-  }();
-  return v;
-}
-
-// Units are counted in 32-bit integers on the device.
-static bool units_fit(long long B, long long per_batch) {
-  return B * per_batch < (1LL << 30);
-}
-
-static void fill_workspace(KParams &P, void *ws, const Layout &L) {
-  P.ws = static_cast<char *>(ws);
-  char *w = static_cast<char *>(ws) + kPassHeaderBytes;
-  P.hdr = reinterpret_cast<WsHeader *>(w);
-  P.a_count = reinterpret_cast<unsigned *>(w + L.a_count);
-  P.b_count = reinterpret_cast<unsigned *>(w + L.b_count);
-  P.flag = reinterpret_cast<unsigned *>(w + L.flag);
-  P.err = reinterpret_cast<int *>(w + L.err);
-  P.ctrl_bytes = L.ctrl;
-  P.dec = reinterpret_cast<Decision *>(w + L.dec);
-  P.partA = reinterpret_cast<float2 *>(w + L.partA);
-  P.partB = reinterpret_cast<float *>(w + L.partB);
-  P.tiles = L.tiles;
-}
-
 static std::atomic<unsigned long long> g_calls{0};
+static std::atomic<int> g_force_stream{0};
+
+bool force_stream_path() { return g_force_stream.load(std::memory_order_relaxed) != 0; }
 
 unsigned long long next_call_id() {
   return g_calls.fetch_add(1, std::memory_order_relaxed) + 1;
@@ -104,11 +75,9 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt, cons
       !aligned_to(out_row_status, 4) || !aligned_to(out_diag, 16))
     return SV_ERR_INVALID_ARG;
   const int rows = (gamma + 1) + (probs ? 0 : gamma);
-  const Layout L = make_layout(B, rows, V);
   if (workspace_bytes < workspace_bytes_any(B, rows, V) ||
       (reinterpret_cast<uintptr_t>(workspace) & 15))
     return SV_ERR_INVALID_ARG;
-  if (!units_fit(B, (long long)rows * L.tiles)) return SV_ERR_UNSUPPORTED;
 
   KParams P{};
   P.target = target_logits;
@@ -120,13 +89,11 @@ SV_API sv_status spec_verify_chain(const void *target_logits, sv_dtype tdt, cons
   P.gamma = gamma;
   P.V = V;
   P.rows = rows;
-  P.phase_b = 1;
-  P.use_stream = stream_enabled();
   P.out_tokens = out_tokens;
   P.out_nacc = out_num_accepted;
   P.out_diag = out_diag;
   P.out_status = out_row_status;
-  fill_workspace(P, workspace, L);
+  P.ws = static_cast<char *>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (tdt) {
     case SV_F32: return launch_chain_f32(P, ddt, probs, s);
@@ -151,11 +118,9 @@ SV_API sv_status spec_verify_chain_greedy(const void *target_logits, sv_dtype td
       !aligned_to(out_row_status, 4))
     return SV_ERR_INVALID_ARG;
   const int rows = gamma + 1;
-  const Layout L = make_layout(B, rows, V);
   if (workspace_bytes < workspace_bytes_any(B, rows, V) ||
       (reinterpret_cast<uintptr_t>(workspace) & 15))
     return SV_ERR_INVALID_ARG;
-  if (!units_fit(B, (long long)rows * L.tiles)) return SV_ERR_UNSUPPORTED;
 
   KParams P{};
   P.target = target_logits;
@@ -164,12 +129,10 @@ SV_API sv_status spec_verify_chain_greedy(const void *target_logits, sv_dtype td
   P.gamma = gamma;
   P.V = V;
   P.rows = rows;
-  P.phase_b = 0;
-  P.use_stream = stream_enabled();
   P.out_tokens = out_tokens;
   P.out_nacc = out_num_accepted;
   P.out_status = out_row_status;
-  fill_workspace(P, workspace, L);
+  P.ws = static_cast<char *>(workspace);
   return launch_chain_greedy(P, tdt, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -190,11 +153,9 @@ SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
       !aligned_to(node_tokens, 4) || !aligned_to(out_path, 4) || !aligned_to(out_tokens, 4) ||
       !aligned_to(out_num_accepted, 4) || !aligned_to(out_row_status, 4))
     return SV_ERR_INVALID_ARG;
-  const Layout L = make_layout(B, N, V);
   if (workspace_bytes < workspace_bytes_any(B, N, V) ||
       (reinterpret_cast<uintptr_t>(workspace) & 15))
     return SV_ERR_INVALID_ARG;
-  if (!units_fit(B, (long long)N * L.tiles)) return SV_ERR_UNSUPPORTED;
 
   KParams P{};
   P.target = node_logits;
@@ -205,13 +166,11 @@ SV_API sv_status spec_verify_tree_greedy(const void *node_logits, sv_dtype dt,
   P.V = V;
   P.rows = N;
   P.max_depth = max_depth;
-  P.phase_b = 0;
-  P.use_stream = stream_enabled();
   P.out_path = out_path;
   P.out_tokens = out_tokens;
   P.out_nacc = out_num_accepted;
   P.out_status = out_row_status;
-  fill_workspace(P, workspace, L);
+  P.ws = static_cast<char *>(workspace);
   return launch_tree(P, dt, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -226,9 +185,7 @@ SV_API sv_status spec_draft_sample(const void *logits, sv_dtype dt, const float 
   if (!aligned_to(temperatures, 4) || !aligned_to(uniforms, 4) || !aligned_to(out_tokens, 4) ||
       !aligned_to(out_probs, 4) || !aligned_to(out_row_status, 4))
     return SV_ERR_INVALID_ARG;
-  // rows must start on 16-byte boundaries (the streaming path only)
-  if ((reinterpret_cast<uintptr_t>(logits) & 15) || ((size_t)V * dtype_size(dt)) % 16)
-    return SV_ERR_UNSUPPORTED;
+  if (!aligned_to(logits, dtype_size(dt))) return SV_ERR_INVALID_ARG;
   if (workspace_bytes < workspace_bytes_any(B, 1, V) ||
       (reinterpret_cast<uintptr_t>(workspace) & 15))
     return SV_ERR_INVALID_ARG;
@@ -240,12 +197,15 @@ SV_API sv_status spec_draft_sample(const void *logits, sv_dtype dt, const float 
   P.N = 1;
   P.V = V;
   P.rows = 1;
-  P.use_stream = 1;
   P.out_tokens = out_tokens;
   P.out_diag = out_probs;
   P.out_status = out_row_status;
-  fill_workspace(P, workspace, make_layout(B, 1, V));
+  P.ws = static_cast<char *>(workspace);
   return launch_draft(P, dt, reinterpret_cast<cudaStream_t>(stream));
+}
+
+SV_API int spec_verify_force_stream_path(int on) {
+  return g_force_stream.exchange(on ? 1 : 0, std::memory_order_relaxed);
 }
 
 SV_API unsigned long long spec_verify_set_call_counter(unsigned long long calls) {

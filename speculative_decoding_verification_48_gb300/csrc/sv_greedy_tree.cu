@@ -21,15 +21,15 @@ sv_status launch_tree(const KParams &P, sv_dtype dt, cudaStream_t stream) {
   return SV_ERR_UNSUPPORTED;
 }
 
-// Draft-side draws: the two-launch path only (rows start on 16-byte
-// boundaries, checked by the caller).
+// Draft-side draws: the two-launch path, whatever the rows' alignment.
 template <int DT>
 static sv_status launch_draft_t(const KParams &P, cudaStream_t stream) {
   constexpr int es = (DT == SV_F32) ? 4 : 2;
-  const PassLayout L = make_pass_layout(P.B, 1, P.V, es, es, false);
+  const bool unaligned = !rows_aligned(P.target, P.V, es);
+  const PassLayout L = make_pass_layout(P.B, 1, P.V, es, es, false, unaligned);
   const long long total = pass_units<MODE_DRAFT, DT, DT, false>(P, L);
   if (total < 0) return SV_ERR_UNSUPPORTED;
-  return launch_pass<MODE_DRAFT, DT, DT, false>(P, L, total, stream);
+  return launch_pass<MODE_DRAFT, DT, DT, false>(P, L, total, unaligned, stream);
 }
 
 sv_status launch_draft(const KParams &P, sv_dtype dt, cudaStream_t stream) {

@@ -1,6 +1,6 @@
 // Internal definitions shared by the host API and the kernels of the
-// verification library: tile geometry, workspace layout, kernel parameters
-// and the unit schedule.
+// verification library: the verification modes, the parameters of a call
+// and the launchers.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,101 +11,29 @@
 
 namespace sv {
 
-// One CTA processes one "unit": a tile of kTile consecutive vocabulary
-// entries of one logit row (Phase A), or of one target/draft row pair
-// (Phase B).  256 threads x 32 elements per thread.
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kTile = 8192;
-constexpr int kPer = kTile / kThreads;
 constexpr int kMaxRows = 2 * SV_MAX_GAMMA + 1;
 
 enum Mode { MODE_CHAIN = 0, MODE_CHAIN_GREEDY = 1, MODE_TREE = 2, MODE_DRAFT = 3 };
-enum DecKind { DEC_DONE = 0, DEC_RESIDUAL = 1 };
-
-// Per-batch-row decision written by the CTA that completes the row's
-// Phase A, read by the row's Phase B units.  64 bytes.
-struct Decision {
-  int kind;    // DecKind
-  int j;       // first rejected position
-  int pad0, pad1;
-  float c;     // log2(e) / T
-  float Mp, invZp, Mq, invZq;  // row maxima and 1 / normalisers of rows p_j, q_j
-  float u;     // the categorical draw u_gamma
-  float pad2[6];
-};
-static_assert(sizeof(Decision) == 64, "Decision must stay 64 bytes");
-
-struct WsHeader {
-  unsigned unit_counter;  // dynamic work counter (reset by the last CTA to exit)
-  unsigned exit_counter;
-};
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// The first kPassHeaderBytes of every workspace hold the two-launch path's
-// state between calls (claim counters and their validity stamp); the
-// register-tile kernels' layout starts after them and never touches them.
+// The first kPassHeaderBytes of every workspace hold state kept valid from
+// call to call (claim counters, error, ready, stamp and epoch words).
 constexpr size_t kPassHeaderBytes = 4096;
 
-// Workspace layout for B batch rows of `rows` logit rows of V entries.  The
-// control block [0, ctrl) holds the work counters, per-row arrival counters,
-// decision flags and error words; every call zeroes it first (one small
-// memset), so a workspace needs no initialisation and may be shared by calls
-// of different shapes in stream order.
-struct Layout {
-  size_t a_count, b_count, flag, err, ctrl, dec, partA, partB, total;
-  int tiles;
-};
-
-inline Layout make_layout(int B, int rows, int V) {
-  Layout L;
-  L.tiles = (V + kTile - 1) / kTile;
-  size_t off = 256;  // WsHeader
-  L.a_count = off; off = align_up(off + (size_t)B * 4, 256);
-  L.b_count = off; off = align_up(off + (size_t)B * 4, 256);
-  L.flag = off;    off = align_up(off + (size_t)B * 4, 256);
-  L.err = off;     off = align_up(off + (size_t)B * 4, 256);
-  L.ctrl = off;
-  L.dec = off;     off = align_up(off + (size_t)B * sizeof(Decision), 256);
-  L.partA = off;   off = align_up(off + (size_t)B * rows * L.tiles * sizeof(float2), 256);
-  L.partB = off;   off = align_up(off + (size_t)B * L.tiles * sizeof(float), 256);
-  L.total = off;
-  return L;
-}
-
-// Unit schedule of one launch.  The unit sequence is built from B blocks
-// (one per batch row, in batch order): block k holds the A units of batch
-// row k followed by the B units of batch row k - L (the lag).  The B units
-// of the last L rows follow the last A block.  With Bc = 0 a launch runs A
-// units only; with A = 0 and L = 0 it runs B units only.
-struct Sched {
-  int B, A, Bc, L;
-  int total;
-};
-
+// One call, as the entry points receive it.
 struct KParams {
-  const void *target;         // chain: [B, gamma+1, V]; tree: [B*N, V]
+  const void *target;         // chain: [B, gamma+1, V]; tree: [B*N, V]; draft: [B, V]
   const void *draft;          // [B, gamma, V] logits or fp32 probabilities
   const int32_t *draft_tokens;
   const float *temps;
   const float *unif;
   const int32_t *parent;
   const int32_t *node_tokens;
-  int B, gamma, V, tiles, rows, N, max_depth;
-  int phase_b;                // 1 if the call has Phase-B units (publish decisions)
-  int use_stream;             // allow the streaming (TMA ring) kernel
+  int B, gamma, V, rows, N, max_depth;
   int32_t *out_tokens, *out_nacc, *out_status, *out_path;
   float *out_diag;
   char *ws;                   // workspace base
-  WsHeader *hdr;
-  unsigned *a_count, *b_count, *flag;
-  int *err;                   // per-row SV_ROW_TIMEOUT bits from Phase-B waits
-  size_t ctrl_bytes;          // bytes of the control block zeroed per call
-  Decision *dec;
-  float2 *partA;
-  float *partB;
-  Sched sched;
 };
 
 // Launchers, defined in the kernel translation units (one per target dtype
@@ -120,7 +48,12 @@ sv_status launch_draft(const KParams &P, sv_dtype dt, cudaStream_t stream);
 // Device properties cached per device (host side).
 int sm_count(int device);
 
-// Workspace bytes covering both kernel families for the given shape.
+// Diagnostics: every call takes the two-launch streaming path (set by
+// spec_verify_force_stream_path).
+bool force_stream_path();
+
+// Workspace bytes covering every call shape with B batch rows of at most
+// `rows` logit rows of V elements.
 size_t workspace_bytes_any(int B, int rows, int V);
 
 // Identifier of a launched call, unique across every entry point and

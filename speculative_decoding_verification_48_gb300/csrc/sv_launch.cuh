@@ -1,10 +1,11 @@
-// Host-side launches: the two-launch path for 16-byte-aligned rows, the
-// register-tile kernels (two phases) for any other shape.
+// Host-side launches of the two-launch path (the stats kernel, then the
+// decide kernel as its programmatic dependent) for every entry point, dtype
+// and row alignment.
 #pragma once
 
 #include <atomic>
 
-#include "sv_pass_decide.cuh"
+#include "sv_cluster.cuh"
 
 namespace sv {
 
@@ -25,33 +26,6 @@ inline unsigned partial_tag(unsigned long long call_id) {
   return (unsigned)((call_id << 1) | 1ull) * 0x9E3779B1u;
 }
 
-// Launches one instantiation with the call's schedule.  The grid is one
-// wave of resident CTAs (SM count x occupancy), capped by the unit count;
-// CTAs pull units from the workspace counter.
-template <int MODE, int TDT, int DDT, bool PROBS, int PHASES>
-sv_status launch_phase(const KParams &P0, const Sched &s, cudaStream_t stream) {
-  if (s.total <= 0) return SV_OK;
-  auto kern = sv_verify_kernel<MODE, TDT, DDT, PROBS, PHASES>;
-  static std::atomic<int> occ_cache[kMaxDevices];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
-  int occ = occ_cache[dev].load(std::memory_order_relaxed);
-  if (occ == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, 0) != cudaSuccess ||
-        occ <= 0)
-      return SV_ERR_CUDA;
-    occ_cache[dev].store(occ, std::memory_order_relaxed);
-  }
-  const int sms = sm_count(dev);
-  if (sms <= 0) return SV_ERR_CUDA;
-  const long long cap = (long long)sms * occ;
-  KParams P = P0;
-  P.sched = s;
-  const int grid = (int)(s.total < cap ? s.total : cap);
-  kern<<<grid, kThreads, 0, stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
-}
-
 // Stats units (warp-chunks) of the two-launch path for this call; -1 if the
 // count does not fit the kernels' 32-bit unit indices.
 template <int MODE, int TDT, int DDT, bool PROBS>
@@ -65,11 +39,12 @@ long long pass_units(const KParams &P, const PassLayout &L) {
 // Two-launch path: the stats kernel over every needed row, then the decide
 // kernel as its programmatic dependent (its CTAs launch while the stats
 // kernel drains and wait on the device for its completion).
-template <int MODE, int TDT, int DDT, bool PROBS>
-sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
-                      cudaStream_t stream) {
-  auto stats = sv_stats_kernel<MODE, TDT, DDT, PROBS>;
-  auto decide = sv_decide_kernel<MODE, TDT, DDT, PROBS>;
+template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
+sv_status launch_pass_t(const KParams &P0, const PassLayout &L, long long total,
+                        cudaStream_t stream) {
+  constexpr bool unaligned = UNAL;
+  auto stats = sv_stats_kernel<MODE, TDT, DDT, PROBS, UNAL>;
+  auto decide = sv_decide_kernel<MODE, TDT, DDT, PROBS, UNAL>;
   static std::atomic<int> occ_cache[kMaxDevices], occd_cache[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
@@ -106,6 +81,7 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   S.cD = L.cD;
   S.cMax = L.cMax;
   S.cR = L.cR;
+  S.unaligned = unaligned ? 1 : 0;
   int H = 1;
   if (MODE == MODE_CHAIN) {
     // about 8 residual chunks per decide CTA (one per warp), while the
@@ -191,36 +167,176 @@ sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total,
   return SV_OK;
 }
 
-// Rows of both logit arrays start on 16-byte boundaries.
+// Rows on the 16-byte grid and rows off it run separate instantiations, so
+// the aligned one carries no edge masks.
+template <int MODE, int TDT, int DDT, bool PROBS>
+sv_status launch_pass(const KParams &P0, const PassLayout &L, long long total, bool unaligned,
+                      cudaStream_t stream) {
+  return unaligned ? launch_pass_t<MODE, TDT, DDT, PROBS, true>(P0, L, total, stream)
+                   : launch_pass_t<MODE, TDT, DDT, PROBS, false>(P0, L, total, stream);
+}
+
+// Every row of an array starts on a 16-byte boundary.
 inline bool rows_aligned(const void *p, int V, int es) {
   return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0 && ((size_t)V * es) % 16 == 0;
+}
+
+// The cluster path's shape for a call, if it takes that path: CS CTAs per
+// batch row (or tree), S vocabulary entries per CTA, rstride bytes per kept
+// row slice, dynamic shared memory bytes.  Every cluster of the call must be
+// resident at once (cudaOccupancyMaxActiveClusters, asked once per device
+// and cluster size with the most shared memory a call of the kernel takes).
+// Chains: every kept slice fits kClusterSmemMax.  Trees: rows on 16-byte
+// boundaries, at most kClusterTreeBytesMax of node rows in the call and at
+// most 1 MB of node-row slices per CTA.
+struct ClusterPlan {
+  int CS, S, rstride;
+  size_t smem;
+};
+
+constexpr size_t kTreeUnitSmemMax = 16 * 1024;  // tree unit partials per CTA
+constexpr long long kClusterTreeBytesMax = 8LL << 20;  // node-row bytes of a cluster-path call
+
+template <int MODE, int TDT, int DDT, bool PROBS>
+void *cluster_kernel() {
+  if constexpr (MODE == MODE_TREE)
+    return reinterpret_cast<void *>(sv_cluster_tree_kernel<TDT>);
+  else
+    return reinterpret_cast<void *>(sv_cluster_chain_kernel<MODE, TDT, DDT, PROBS>);
+}
+
+// Clusters of CS CTAs (CS = 1, 2, 4, 8 -> slot 0..3) that fit on the device
+// at once; 0 if the kernel cannot be set up.
+template <int MODE, int TDT, int DDT, bool PROBS>
+int cluster_capacity(int dev, int slot) {
+  static std::atomic<int> cache[kMaxDevices][4];
+  int v = cache[dev][slot].load(std::memory_order_relaxed);
+  if (v != 0) return v > 0 ? v : 0;
+  const void *kern = cluster_kernel<MODE, TDT, DDT, PROBS>();
+  const size_t smem = MODE == MODE_TREE ? kTreeUnitSmemMax : (size_t)kClusterSmemMax;
+  int n = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+      cudaSuccess) {
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = 1u << slot;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(1u << slot);
+    cfg.blockDim = dim3(kPassThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  }
+  if (n <= 0) (void)cudaGetLastError();
+  cache[dev][slot].store(n > 0 ? n : -1, std::memory_order_relaxed);
+  return n > 0 ? n : 0;
+}
+
+template <int MODE, int TDT, int DDT, bool PROBS>
+bool cluster_plan(const KParams &P, int dev, ClusterPlan &cp) {
+  if (force_stream_path() || dev < 0 || dev >= kMaxDevices) return false;
+  constexpr int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
+  if (MODE == MODE_TREE) {
+    // larger calls stream faster over every SM with the two-launch path
+    if (!rows_aligned(P.target, P.V, esT) || P.N > SV_MAX_TREE_NODES ||
+        (long long)P.B * P.N * P.V * esT > kClusterTreeBytesMax)
+      return false;
+    constexpr int E = Chunk<TDT>::kElems;
+    for (int slot = 3; slot >= 0; --slot) {
+      const int CS = 1 << slot;
+      const int S = (int)align_up((size_t)((P.V + CS - 1) / CS), 8);
+      const size_t smem = (size_t)P.N * ((S + E - 1) / E) * sizeof(float2);
+      if ((long long)P.N * S * esT > (1LL << 20) || smem > kTreeUnitSmemMax) return false;
+      if (P.B > cluster_capacity<MODE, TDT, DDT, PROBS>(dev, slot)) continue;
+      cp = ClusterPlan{CS, S, 0, smem};
+      return true;
+    }
+    return false;
+  }
+  if (MODE != MODE_CHAIN && MODE != MODE_CHAIN_GREEDY) return false;
+  const int es = esT > esD ? esT : esD;
+  const int keep = MODE == MODE_CHAIN ? 2 * P.gamma + 1 : P.gamma + 1;
+  for (int slot = 0; slot <= 3; ++slot) {
+    const int CS = 1 << slot;
+    const int S = (int)align_up((size_t)((P.V + CS - 1) / CS), 8);
+    const int rstride = (int)align_up((size_t)S * es, 16);
+    if ((long long)keep * rstride > kClusterSmemMax) continue;
+    if (P.B > cluster_capacity<MODE, TDT, DDT, PROBS>(dev, slot)) return false;
+    cp = ClusterPlan{CS, S, rstride, (size_t)keep * rstride};
+    return true;
+  }
+  return false;
+}
+
+// One launch of the cluster path: B clusters of CS CTAs, a programmatic
+// dependent of the work before it in the stream.
+template <int MODE, int TDT, int DDT, bool PROBS>
+sv_status launch_cluster(const KParams &P0, const ClusterPlan &cp, cudaStream_t stream) {
+  ClusterParams C{};
+  C.target = P0.target;
+  C.draft = P0.draft;
+  C.draft_tokens = P0.draft_tokens;
+  C.temps = P0.temps;
+  C.unif = P0.unif;
+  C.parent = P0.parent;
+  C.node_tokens = P0.node_tokens;
+  C.B = P0.B;
+  C.gamma = P0.gamma;
+  C.V = P0.V;
+  C.N = P0.N;
+  C.max_depth = P0.max_depth;
+  C.S = cp.S;
+  C.rstride = cp.rstride;
+  C.out_tokens = P0.out_tokens;
+  C.out_nacc = P0.out_nacc;
+  C.out_status = P0.out_status;
+  C.out_path = P0.out_path;
+  C.out_diag = P0.out_diag;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cp.CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(P0.B * cp.CS));
+  cfg.blockDim = dim3(kPassThreads);
+  cfg.dynamicSmemBytes = cp.smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if constexpr (MODE == MODE_TREE)
+    return cudaLaunchKernelEx(&cfg, sv_cluster_tree_kernel<TDT>, C) == cudaSuccess ? SV_OK
+                                                                                   : SV_ERR_CUDA;
+  else
+    return cudaLaunchKernelEx(&cfg, sv_cluster_chain_kernel<MODE, TDT, DDT, PROBS>, C) ==
+                   cudaSuccess
+               ? SV_OK
+               : SV_ERR_CUDA;
 }
 
 template <int MODE, int TDT, int DDT, bool PROBS>
 sv_status launch_verify(const KParams &P, cudaStream_t stream) {
   {
-    constexpr int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
-    bool ok = rows_aligned(P.target, P.V, esT);
-    if (MODE == MODE_CHAIN) ok = ok && rows_aligned(P.draft, P.V, esD);
-    if (ok && P.use_stream) {
-      const PassLayout L =
-          make_pass_layout(P.B, P.rows, P.V, esT, esD, MODE == MODE_CHAIN && !PROBS);
-      const long long total = pass_units<MODE, TDT, DDT, PROBS>(P, L);
-      if (total >= 0 && (long long)P.B * 16 < (1LL << 31))
-        return launch_pass<MODE, TDT, DDT, PROBS>(P, L, total, stream);
-    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+    ClusterPlan cp;
+    if (cluster_plan<MODE, TDT, DDT, PROBS>(P, dev, cp))
+      return launch_cluster<MODE, TDT, DDT, PROBS>(P, cp, stream);
   }
-  const int B = P.B, A = P.rows * P.tiles;
-  if (cudaMemsetAsync(P.hdr, 0, P.ctrl_bytes, stream) != cudaSuccess) return SV_ERR_CUDA;
-  if constexpr (MODE == MODE_CHAIN) {
-    // Phase A (+ decisions), then Phase B (+ finalisation) in stream order.
-    const int Bc = P.tiles;
-    const sv_status st =
-        launch_phase<MODE, TDT, DDT, PROBS, 1>(P, Sched{B, A, 0, B, B * A}, stream);
-    if (st != SV_OK) return st;
-    return launch_phase<MODE, TDT, DDT, PROBS, 2>(P, Sched{B, 0, Bc, 0, B * Bc}, stream);
-  }
-  return launch_phase<MODE, TDT, DDT, PROBS, 1>(P, Sched{B, A, 0, B, B * A}, stream);
+  constexpr int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
+  const bool stream_draft = MODE == MODE_CHAIN && !PROBS;
+  // (the residual sweep also reads probability drafts by vectors)
+  const bool unaligned = !rows_aligned(P.target, P.V, esT) ||
+                         (MODE == MODE_CHAIN && !rows_aligned(P.draft, P.V, esD));
+  const PassLayout L = make_pass_layout(P.B, P.rows, P.V, esT, esD, stream_draft, unaligned);
+  const long long total = pass_units<MODE, TDT, DDT, PROBS>(P, L);
+  if (total < 0 || (long long)P.B * 16 >= (1LL << 31)) return SV_ERR_UNSUPPORTED;
+  return launch_pass<MODE, TDT, DDT, PROBS>(P, L, total, unaligned, stream);
 }
 
 template <int TDT>

@@ -1,6 +1,6 @@
-// Shared definitions of the two-launch verification path for rows that start
-// on 16-byte boundaries: chunk geometry, parameters, workspace layout, vector
-// loads and warp-level merge / crossing helpers.
+// Shared definitions of the two-launch verification path: chunk geometry,
+// parameters, workspace layout, vector loads and warp-level merge /
+// crossing helpers.
 //
 //   sv_stats_kernel   streams every logit row once.  Each warp reduces
 //                     "warp-chunks" of 4 KB (32 lanes x 8 x 16-byte vectors)
@@ -15,7 +15,7 @@
 //                     last of them finds the crossing chunk and rescans it.
 #pragma once
 
-#include "sv_kernel.cuh"
+#include "sv_device.cuh"
 
 namespace sv {
 
@@ -103,6 +103,7 @@ struct PassParams {
   Part *part;        // [B][rows][cMax] warp-chunk partials
   unsigned part_tag; // odd, from the host's call id: marks this call's partials
   int poll;          // 1: the decide kernel merges as partials arrive (large calls)
+  int unaligned;     // 1: some streamed row does not start on a 16-byte boundary
   float *resid;      // [B][cR] residual mass per chunk of the rejected row pair
 };
 
@@ -131,12 +132,17 @@ struct PassLayout {
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-inline PassLayout make_pass_layout(int B, int rows, int V, int esT, int esD, bool stream_draft) {
+// Rows off the 16-byte grid are read on the 16-byte grid of their own
+// address: a row's first chunk starts up to one vector before the row, so it
+// may take one chunk more (and its pair sweep one residual chunk more).
+inline PassLayout make_pass_layout(int B, int rows, int V, int esT, int esD, bool stream_draft,
+                                   bool unaligned) {
   PassLayout L;
-  L.cT = ceil_div(V, kChunkBytes / esT);
-  L.cD = stream_draft ? ceil_div(V, kChunkBytes / esD) : 0;
+  const int esR = esT > esD ? esT : esD;
+  L.cT = ceil_div(V + (unaligned ? 16 / esT - 1 : 0), kChunkBytes / esT);
+  L.cD = stream_draft ? ceil_div(V + (unaligned ? 16 / esD - 1 : 0), kChunkBytes / esD) : 0;
   L.cMax = L.cT > L.cD ? L.cT : L.cD;
-  L.cR = ceil_div(V, kResidBytes / (esT > esD ? esT : esD));
+  L.cR = ceil_div(V + (unaligned ? 16 / esR - 1 : 0), kResidBytes / esR);
   L.claim = 0;
   L.err = (size_t)kClaimStripes * kClaimStride * 4;
   L.ready = L.err + 128;
@@ -224,20 +230,15 @@ template <int DT, int VEC> struct RawVec {
   __device__ __forceinline__ void unpack(float *o) const { Elt<DT>::unpack(r, o); }
 };
 
-// Residual term max(0, p(x) - q(x)) of the sweep, with each side's
-// normaliser folded into its exponent: p(x) = 2^(l_p(x) c + a_p),
-// a_p = -(M_p c + log2 Z_p), one FFMA and one ex2 per side (q is read as
-// given for probability drafts).  Identical rows give identical p and q,
-// hence exactly zero; NaN propagates.
+// Residual term max(0, p(x) - q(x)) of the sweep: p(x) = 2^((l_p(x) - M_p) c
+// - log2 Z_p), one FADD, one FFMA and one ex2 per side (q is read as given
+// for probability drafts).  The row maximum is subtracted before the scale,
+// so the exponent of an element near the maximum is small and exact to a
+// few ulp even at a tiny temperature (large c).  Identical rows give
+// identical p and q, hence exactly zero; NaN propagates.
 struct ResidCoef {
-  float c, ap, aq;
+  float c, Mp, lzp, Mq, lzq;  // scale, then each side's maximum and log2 normaliser
 };
-template <bool PROBS>
-__device__ __forceinline__ float resid_term(float lp, float lq, const ResidCoef &k) {
-  const float p = ex2(fmaf(lp, k.c, k.ap));
-  const float q = PROBS ? lq : ex2(fmaf(lq, k.c, k.aq));
-  return max_nan(0.f, p - q);
-}
 
 // Packed pairs of fp32 (sm_100+ two-wide FMA / ADD): one instruction for
 // two lanes of work.
@@ -263,19 +264,21 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
   return r;
 }
 
-// resid_term for two neighbouring elements through the two-wide FMA: the
-// same values as two resid_term calls (fma.rn per lane, p - q rounded once).
+// The residual term for two neighbouring elements through the two-wide
+// FADD and FMA (rounded per lane, p - q rounded once).
 template <bool PROBS>
 __device__ __forceinline__ float2 resid_pair(float lp0, float lp1, float lq0, float lq1,
                                              const ResidCoef &k) {
   const unsigned long long c2 = f2_pack(k.c, k.c);
-  const float2 pe = f2_unpack(f2_fma(f2_pack(lp0, lp1), c2, f2_pack(k.ap, k.ap)));
+  const unsigned long long dp = f2_add(f2_pack(lp0, lp1), f2_pack(-k.Mp, -k.Mp));
+  const float2 pe = f2_unpack(f2_fma(dp, c2, f2_pack(-k.lzp, -k.lzp)));
   const unsigned long long p2 = f2_pack(ex2(pe.x), ex2(pe.y));
   unsigned long long q2;
   if (PROBS) {
     q2 = f2_pack(lq0, lq1);
   } else {
-    const float2 qe = f2_unpack(f2_fma(f2_pack(lq0, lq1), c2, f2_pack(k.aq, k.aq)));
+    const unsigned long long dq = f2_add(f2_pack(lq0, lq1), f2_pack(-k.Mq, -k.Mq));
+    const float2 qe = f2_unpack(f2_fma(dq, c2, f2_pack(-k.lzq, -k.lzq)));
     q2 = f2_pack(ex2(qe.x), ex2(qe.y));
   }
   const float2 d = f2_unpack(f2_fma(q2, f2_pack(-1.f, -1.f), p2));  // p - q

@@ -49,6 +49,33 @@ static __device__ __noinline__ void pass_error_row(const PassParams &P, int b, i
   }
 }
 
+// Bits of one vector of VEC elements of a row at vocabulary index x, read
+// one element at a time: elements inside [0, V) are loaded, the others get
+// the bits `pad` (a packed element pattern).
+template <int DT, int VEC>
+__device__ __forceinline__ typename RawVec<DT, VEC>::R raw_elements(const typename Elt<DT>::T *row,
+                                                                    int x, int V, unsigned pad) {
+  typename RawVec<DT, VEC>::R r;
+  unsigned *w = reinterpret_cast<unsigned *>(&r);
+  constexpr int W = (int)(sizeof(r) / 4);
+  if constexpr (DT == SV_F32) {
+#pragma unroll
+    for (int i = 0; i < W; ++i)
+      w[i] = (x + i >= 0 && x + i < V) ? __ldg(reinterpret_cast<const unsigned *>(row) + x + i)
+                                       : pad;
+  } else {
+    const unsigned short *h = reinterpret_cast<const unsigned short *>(row);
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      const int xa = x + 2 * i, xb = xa + 1;
+      const unsigned a = (xa >= 0 && xa < V) ? __ldg(h + xa) : (pad & 0xffffu);
+      const unsigned bb = (xb >= 0 && xb < V) ? __ldg(h + xb) : (pad >> 16);
+      w[i] = a | (bb << 16);
+    }
+  }
+  return r;
+}
+
 // Chain rows.  Every CTA of the row merges the partials it needs and makes
 // the decision (cheap, from L2); CTA h = 0 writes the diagnostics and, for
 // greedy, bonus and invalid rows, the outputs.  A rejected row's residual
@@ -56,7 +83,7 @@ static __device__ __noinline__ void pass_error_row(const PassParams &P, int b, i
 // step issues all of its loads at once, so the row costs a handful of
 // dependent round trips: gathers (before the wait on the stats kernel),
 // partials, sweep, arrival, residual sums, rescan.
-template <int MODE, int TDT, int DDT, bool PROBS>
+template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
 __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &sm) {
   using TT = typename Elt<TDT>::T;
   using DTy = typename Elt<DDT>::T;
@@ -216,8 +243,9 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
       tok_j = sm.rowI[j];
     } else {
       const Part *pr = pb + (size_t)g * P.cMax;
-      tok_j = warp_sample_softmax_row<TDT>(tgt + (size_t)g * V, pr, P.cT, V, sm.rowM[g], c,
-                                           ug);
+      const TT *brow = tgt + (size_t)g * V;
+      tok_j = warp_sample_softmax_row<TDT>(brow, pr, P.cT, V, sm.rowM[g], c, ug,
+                                           P.unaligned ? row_offset16<TDT>(brow) : 0);
     }
     for (int s = lane; s < G1; s += 32)
       ot[s] = s < j ? x : (s == j ? tok_j : -1);  // lane s holds draft token s
@@ -227,15 +255,29 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     }
     return;
   }
-  // 4. residual sweep of the row pair (p_j, q_j), chunks [c0, c1) of this CTA
+  // 4. residual sweep of the row pair (p_j, q_j), chunks [c0, c1) of this CTA.
+  // Chunk ch covers vocabulary indices [ch kElems - off, (ch + 1) kElems -
+  // off), off being the target row's elements before its first vector
+  // boundary (0 when rows start on 16-byte boundaries), so the target row's
+  // vectors are aligned; the draft row's are too when its own offset agrees,
+  // else its elements are read one at a time.  Slots outside the row are
+  // masked: p = 0 there, so they add no mass.
   using PC = PairChunk<TDT, DDT>;
+  using RA = RawVec<TDT, PC::kVec>;
+  using RQ = RawVec<DDT, PC::kVec>;
   ResidCoef rk;
   rk.c = c;
-  rk.ap = -fmaf(sm.rowM[j], c, log2f(sm.rowZ[j]));
-  rk.aq = PROBS ? 0.f : -fmaf(sm.rowM[G1 + j], c, log2f(sm.rowZ[G1 + j]));
+  rk.Mp = sm.rowM[j];
+  rk.lzp = log2f(sm.rowZ[j]);
+  rk.Mq = PROBS ? 0.f : sm.rowM[G1 + j];
+  rk.lzq = PROBS ? 0.f : log2f(sm.rowZ[G1 + j]);
   const float Mp = sm.rowM[j];
   const TT *prow = tgt + (size_t)j * V;
   const DTy *qrow = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V;
+  const int off = UNAL ? (int)((reinterpret_cast<uintptr_t>(prow) & (RA::kB - 1)) / sizeof(TT))
+                       : 0;
+  const bool qa = !UNAL || (reinterpret_cast<uintptr_t>(qrow - off) & (RQ::kB - 1)) == 0;
+  const unsigned padq = PROBS ? 0u : neg_inf_word<DDT>();
   float *rs = P.resid + (size_t)b * P.cR;
   const int c0 = (int)((long long)h * P.cR / P.H), c1 = (int)((long long)(h + 1) * P.cR / P.H);
   // Each warp takes chunk pairs (ch, ch + 8), ch = c0 + warp + 16 i: the
@@ -243,21 +285,27 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   // warp's shared-memory stage by cp.async, and both are in flight before the
   // first residual term (one memory round trip per pair).  Every lane reads
   // back only the vectors it copied itself, so its own wait suffices.
-  using RA = RawVec<TDT, PC::kVec>;
-  using RQ = RawVec<DDT, PC::kVec>;
   typename RA::R *sa = reinterpret_cast<typename RA::R *>(sm.stage[warp]);
   typename RQ::R *sq = reinterpret_cast<typename RQ::R *>(sm.stage[warp] + kResidBytes);
   RA ra[PC::kVecs];
   RQ rq[PC::kVecs];
-  auto chunk_sum = [&](int n) {
+  auto chunk_sum = [&](int x0) {
     unsigned long long s2 = 0ull;  // (+0, +0)
 #pragma unroll
     for (int u = 0; u < PC::kVecs; ++u) {
-      const int e = (lane + 32 * u) * PC::kVec;
-      if (e < n) {
+      const int x = x0 + (lane + 32 * u) * PC::kVec;
+      if (x < V && (!UNAL || x + PC::kVec > 0)) {
         float a[PC::kVec], q[PC::kVec];
         ra[u].unpack(a);
         rq[u].unpack(q);
+        if (UNAL && (x < 0 || x + PC::kVec > V)) {
+#pragma unroll
+          for (int t = 0; t < PC::kVec; ++t)
+            if (x + t < 0 || x + t >= V) {
+              a[t] = -CUDART_INF_F;  // p = 0: no mass
+              q[t] = PROBS ? 0.f : -CUDART_INF_F;  // a neighbour's NaN stays out
+            }
+        }
 #pragma unroll
         for (int t = 0; t < PC::kVec; t += 2) {
           const float2 r = resid_pair<PROBS>(a[t], a[t + 1], q[t], q[t + 1], rk);
@@ -270,45 +318,48 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   };
   // 8-byte vectors (a 16-bit target beside fp32 draft rows) measured slower
   // staged than one register-held chunk at a time, so only pairs of 16-byte
-  // vectors take the stage
-  constexpr bool kStage = RA::kB == 16 && RQ::kB == 16;
-  for (int ch = c0 + warp; ch < c1; ch += (kStage ? 2 : 1) * kPassWarps) {
+  // vectors take the stage, and only when both rows' vectors are aligned
+  const bool stage = RA::kB == 16 && RQ::kB == 16 && qa;
+  const int stride = (stage ? 2 : 1) * kPassWarps;
+  for (int ch = c0 + warp; ch < c1; ch += stride) {
     const int chB = ch + kPassWarps;
-    const int nB = kStage && chB < c1 ? min(PC::kElems, V - chB * PC::kElems) : 0;
-    if (nB > 0) {
-      const int xB = chB * PC::kElems;
+    const bool useB = stage && chB < c1;
+    if (useB) {
+      const int xB = chB * PC::kElems - off;
 #pragma unroll
       for (int u = 0; u < PC::kVecs; ++u) {
-        const int e = (lane + 32 * u) * PC::kVec;
-        if (e < nB) {
-          cp_async<RA::kB>(sa + lane + 32 * u, prow + xB + e);
-          cp_async<RQ::kB>(sq + lane + 32 * u, qrow + xB + e);
+        const int x = xB + (lane + 32 * u) * PC::kVec;
+        if (x < V && (!UNAL || x + PC::kVec > 0)) {
+          cp_async<RA::kB>(sa + lane + 32 * u, prow + x);
+          cp_async<RQ::kB>(sq + lane + 32 * u, qrow + x);
         }
       }
       cp_async_commit();
     }
-    const int x0 = ch * PC::kElems;
-    const int n = min(PC::kElems, V - x0);
+    const int x0 = ch * PC::kElems - off;
 #pragma unroll
     for (int u = 0; u < PC::kVecs; ++u) {
-      const int e = (lane + 32 * u) * PC::kVec;
-      if (e < n) {
-        ra[u].load(prow + x0 + e);
-        rq[u].load(qrow + x0 + e);
+      const int x = x0 + (lane + 32 * u) * PC::kVec;
+      if (x < V && (!UNAL || x + PC::kVec > 0)) {
+        ra[u].load(prow + x);
+        if (qa) rq[u].load(qrow + x);
+        else rq[u].r = raw_elements<DDT, PC::kVec>(qrow, x, V, padq);
       }
     }
-    const float s = chunk_sum(n);
+    const float s = chunk_sum(x0);
     if (lane == 0) rs[ch] = s;
-    if (nB > 0) {
+    if (useB) {
       cp_async_wait_all();
+      const int xB = chB * PC::kElems - off;
 #pragma unroll
       for (int u = 0; u < PC::kVecs; ++u) {
-        if ((lane + 32 * u) * PC::kVec < nB) {
+        const int x = xB + (lane + 32 * u) * PC::kVec;
+        if (x < V && (!UNAL || x + PC::kVec > 0)) {
           ra[u].r = sa[lane + 32 * u];
           rq[u].r = sq[lane + 32 * u];
         }
       }
-      const float sB = chunk_sum(nB);
+      const float sB = chunk_sum(xB);
       if (lane == 0) rs[chB] = sB;
     }
   }
@@ -340,7 +391,8 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     if (warp != 0) return;
     if (!(R > 0.f) && !isnan(R)) {
       // no residual mass (p_j == q_j up to rounding): draw from p_j
-      const int k = warp_sample_softmax_row<TDT>(prow, pb + (size_t)j * P.cMax, P.cT, V, Mp, c, u);
+      const int k = warp_sample_softmax_row<TDT>(prow, pb + (size_t)j * P.cMax, P.cT, V, Mp, c, u,
+                                                 P.unaligned ? row_offset16<TDT>(prow) : 0);
       for (int s = lane; s < G1; s += 32)
         ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
       if (lane == 0) {
@@ -356,11 +408,10 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
   const float target = u * R;
   constexpr int SUB = PC::kElems / kPassWarps, SPER = SUB / 32;
   static_assert(SPER % 2 == 0, "pairs of elements per lane");
-  const int xs = t * PC::kElems + warp * SUB;
-  const int ns = min(SUB, V - xs);  // at most 0 past the row's end: all padding
+  const int xs = t * PC::kElems - off + warp * SUB;
   float a[SPER], qv[SPER];
-  lane_consecutive_load<TDT, SPER>(prow + xs, ns, -CUDART_INF_F, a);
-  lane_consecutive_load<DDT, SPER>(qrow + xs, ns, PROBS ? 0.f : -CUDART_INF_F, qv);
+  lane_row_load<TDT, SPER>(prow, xs, V, -CUDART_INF_F, a);
+  lane_row_load<DDT, SPER>(qrow, xs, V, PROBS ? 0.f : -CUDART_INF_F, qv);
   float ls = 0.f;
   int lpos = -1;
 #pragma unroll
@@ -521,7 +572,8 @@ __device__ void decide_draft_row(const PassParams &P, int b) {
     if (!(mz.y > 0.f && mz.y <= 3.0e38f)) {
       status = SV_ROW_NONFINITE;
     } else {
-      tok = warp_sample_softmax_row<DT>(row, pr, P.cT, V, mz.x, c, __ldg(P.unif + b));
+      tok = warp_sample_softmax_row<DT>(row, pr, P.cT, V, mz.x, c, __ldg(P.unif + b),
+                                        P.unaligned ? row_offset16<DT>(row) : 0);
       prob = ex2((Elt<DT>::load1(row + tok) - mz.x) * c) / mz.y;
     }
   }
@@ -533,7 +585,7 @@ __device__ void decide_draft_row(const PassParams &P, int b) {
   }
 }
 
-template <int MODE, int TDT, int DDT, bool PROBS>
+template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
 __global__ void __launch_bounds__(kPassThreads, 4) sv_decide_kernel(const PassParams P) {
   const int b = blockIdx.x / P.H, h = blockIdx.x - b * P.H;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -558,7 +610,7 @@ __global__ void __launch_bounds__(kPassThreads, 4) sv_decide_kernel(const PassPa
     decide_tree<TDT>(P, b, sm);
   } else {
     __shared__ DecideSmem sm;
-    decide_chain_row<MODE, TDT, DDT, PROBS>(P, b, h, sm);
+    decide_chain_row<MODE, TDT, DDT, PROBS, UNAL>(P, b, h, sm);
   }
 }
 

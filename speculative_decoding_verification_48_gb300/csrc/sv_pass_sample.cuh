@@ -1,4 +1,4 @@
-// Inverse-CDF draws for the decide kernel: crossing search over chunk masses
+// Inverse-CDF draws: crossing search over chunk masses
 // and rescan of the crossing chunk ("論文解説: Speculative Sampling",
 // §修正付き棄却サンプリング; the draw is the inverse CDF in ascending vocabulary
 // order: the smallest k with sum_{x<=k} w(x) > u * sum_x w(x)).
@@ -43,27 +43,28 @@ __device__ __forceinline__ int warp_prefix_cross(int cnt, float target, WF w, fl
   return last_i;
 }
 
-// The lane's PER consecutive elements [lane * PER, lane * PER + PER) of a
-// chunk starting at `base` (16-byte aligned); slots at or past n get `pad`.
+// The lane's PER consecutive elements x0 + lane * PER + k (k < PER) of a row
+// of V elements; elements outside [0, V) get `pad`.  Vector loads when the
+// lane's elements all lie in the row and start on a 16-byte boundary,
+// otherwise one element at a time (no byte outside the row is read).
 template <int DT, int PER>
-__device__ __forceinline__ void lane_consecutive_load(const typename Elt<DT>::T *base, int n,
-                                                      float pad, float (&v)[PER]) {
+__device__ __forceinline__ void lane_row_load(const typename Elt<DT>::T *row, int x0, int V,
+                                              float pad, float (&v)[PER]) {
   using E = Elt<DT>;
   constexpr int VEC = E::kVec;
-  const int e0 = lane_id() * PER;
-  const typename E::T *p = base + e0;
-  if (e0 + PER <= n) {
-    if constexpr (PER % VEC == 0) {
+  const int xs = x0 + lane_id() * PER;
+  const typename E::T *p = row + xs;
+  bool vec = xs >= 0 && xs + PER <= V;
+  if constexpr (PER % VEC == 0) {
+    vec = vec && (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+    if (vec) {
 #pragma unroll
       for (int k = 0; k < PER / VEC; ++k) E::unpack(ld_nc16(p + k * VEC), &v[k * VEC]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < PER; ++k) v[k] = E::load1(p + k);
+      return;
     }
-  } else {
-#pragma unroll
-    for (int k = 0; k < PER; ++k) v[k] = (e0 + k < n) ? E::load1(p + k) : pad;
   }
+#pragma unroll
+  for (int k = 0; k < PER; ++k) v[k] = (xs + k >= 0 && xs + k < V) ? E::load1(row + xs + k) : pad;
 }
 
 // Crossing inside a chunk whose lane-consecutive weights are w[PER]: the
@@ -174,12 +175,16 @@ __device__ __forceinline__ int warp_chunk_cross(int cnt, WF wf, float u, float &
 }
 
 // Draw from softmax row `row` (V elements of DT, max M, scale c) with the
-// stats kernel's chunk partials part[cnt]: the chunk masses
+// row's chunk partials part[cnt]: the chunk masses
 // s_i 2^((m_i - M) c) locate the crossing chunk of u * R, then that chunk is
-// rescanned element by element.  Returns a vocabulary index.
+// rescanned element by element.  Chunk i starts at vocabulary index
+// i * kElems - off (off: the row's elements before its first 16-byte
+// boundary, 0 for a row that starts on one).  Returns a vocabulary index.
 template <int DT>
-static __device__ __noinline__ int warp_sample_softmax_row(const typename Elt<DT>::T *row, const Part *part, int cnt,
-                                       int V, float M, float c, float u) {
+static __device__ __noinline__ int warp_sample_softmax_row(const typename Elt<DT>::T *row,
+                                                           const Part *part, int cnt, int V,
+                                                           float M, float c, float u,
+                                                           int off = 0) {
   using C = Chunk<DT>;
   constexpr int HALF = C::kElems / 2, PER = HALF / 32;
   auto wt = [&](int i) {
@@ -190,9 +195,9 @@ static __device__ __noinline__ int warp_sample_softmax_row(const typename Elt<DT
   const int t = warp_chunk_cross(cnt, wt, u, R, base);
   const float target = u * R;
   // rescan the crossing chunk one half at a time (32 values per lane)
-  int x0 = t * C::kElems;
+  int x0 = t * C::kElems - off;
   float v[PER];
-  lane_consecutive_load<DT, PER>(row + x0, min(HALF, V - x0), -CUDART_INF_F, v);
+  lane_row_load<DT, PER>(row, x0, V, -CUDART_INF_F, v);
   float hs = 0.f;
 #pragma unroll
   for (int k = 0; k < PER; ++k) {
@@ -203,7 +208,7 @@ static __device__ __noinline__ int warp_sample_softmax_row(const typename Elt<DT
   if (base + hs <= target && x0 + HALF < V) {
     base += hs;
     x0 += HALF;
-    lane_consecutive_load<DT, PER>(row + x0, min(HALF, V - x0), -CUDART_INF_F, v);
+    lane_row_load<DT, PER>(row, x0, V, -CUDART_INF_F, v);
 #pragma unroll
     for (int k = 0; k < PER; ++k) v[k] = ex2((v[k] - M) * c);
   }

@@ -11,7 +11,14 @@
 // counters (below), so the grid reads one contiguous front of memory and
 // fast warps take more chunks than slow ones.
 // Each warp keeps the next chunk's eight 16-byte loads per lane in flight
-// while it reduces the current one.  For chains the list runs from the last
+// while it reduces the current one.
+//
+// Rows need not start on 16-byte boundaries: a row's chunks lie on the
+// 16-byte grid of its own address (its first chunk starts up to 15 bytes
+// before the row).  Every aligned 16-byte block holding an element of the
+// row is loaded whole, and the slots outside the row are masked when the
+// chunk is reduced.  A block holding a byte of the row never lies on another
+// page, so the loads stay within mapped memory.  For chains the list runs from the last
 // draft position to the first: the rows that the residual sweep is most
 // likely to re-read (early positions, where the first rejection usually
 // falls) are then the most recently read when the sweep starts, and still in
@@ -26,15 +33,23 @@ namespace sv {
 enum ChunkKind { CK_SKIP = 0, CK_SOFTMAX = 1, CK_ARGMAX = 2 };
 
 struct ChunkRef {
-  const void *src;  // first byte of the warp-chunk
+  const void *src;  // first byte of the warp-chunk (16-byte aligned)
   Part *dst;        // its partial
   unsigned tag;     // this call's partial tag
-  int kind, n, x0;  // n valid elements, x0 = first vocabulary index
+  int kind;
+  int x0;           // vocabulary index of the chunk's slot 0 (negative: before the row)
+  int lo, n;        // the slots [lo, n) hold row elements
   int draft;        // 1: element type DDT, else TDT
   float c;
 };
 
-template <int MODE, int TDT, int DDT, bool PROBS>
+// Elements of a row before its first 16-byte boundary (0 on aligned paths).
+template <int DT>
+__device__ __forceinline__ int row_offset16(const void *row) {
+  return (int)((reinterpret_cast<uintptr_t>(row) & 15) / sizeof(typename Elt<DT>::T));
+}
+
+template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
 __device__ __forceinline__ ChunkRef decode_chunk(const PassParams &P, int k) {
   ChunkRef r;
   int b, row, ci, draft = 0, pos = 0;
@@ -65,8 +80,19 @@ __device__ __forceinline__ ChunkRef decode_chunk(const PassParams &P, int k) {
     row = draft ? g + 1 + pos : pos;
   }
   const int E = draft ? Chunk<DDT>::kElems : Chunk<TDT>::kElems;
-  r.x0 = ci * E;
+  const int ES = draft ? Chunk<DDT>::kEs : Chunk<TDT>::kEs;
+  const char *rowp;
+  if (draft) {
+    rowp = static_cast<const char *>(P.draft) + ((size_t)b * P.gamma + pos) * P.V * ES;
+  } else {
+    const int rows_per = (MODE == MODE_TREE || MODE == MODE_DRAFT) ? P.N : P.gamma + 1;
+    rowp = static_cast<const char *>(P.target) + ((size_t)b * rows_per + row) * P.V * ES;
+  }
+  const int off = UNAL ? (int)((reinterpret_cast<uintptr_t>(rowp) & 15) / ES) : 0;
+  r.x0 = ci * E - off;
+  r.lo = ci == 0 ? off : 0;
   r.n = min(E, P.V - r.x0);
+  r.src = rowp + (ptrdiff_t)r.x0 * ES;
   r.draft = draft;
   r.dst = P.part + ((size_t)b * P.rows + row) * P.cMax + ci;
   r.tag = P.part_tag;
@@ -79,14 +105,6 @@ __device__ __forceinline__ ChunkRef decode_chunk(const PassParams &P, int k) {
   } else {
     r.kind = CK_ARGMAX;
   }
-  if (draft) {
-    const auto *d = reinterpret_cast<const typename Elt<DDT>::T *>(P.draft);
-    r.src = d + ((size_t)b * P.gamma + pos) * P.V + r.x0;
-  } else {
-    const auto *t = reinterpret_cast<const typename Elt<TDT>::T *>(P.target);
-    const int rows_per = (MODE == MODE_TREE || MODE == MODE_DRAFT) ? P.N : P.gamma + 1;
-    r.src = t + ((size_t)b * rows_per + row) * P.V + r.x0;
-  }
   return r;
 }
 
@@ -96,10 +114,9 @@ template <int DT> __device__ __forceinline__ unsigned neg_inf_word() {
 }
 
 // The lane's eight 16-byte vectors of a warp-chunk: vector l + 32 u holds
-// bytes [16 (l + 32 u), 16 (l + 32 u) + 16) of the chunk.  Vectors past the
-// row end (n is a multiple of the vector width on this path) are filled
-// with -inf instead of loaded.
-template <int DT>
+// slots [VEC (l + 32 u), VEC (l + 32 u) + VEC).  Vectors with no slot of
+// the row are filled with -inf instead of loaded.
+template <int DT, bool UNAL>
 __device__ __forceinline__ void chunk_issue_t(const ChunkRef &r, uint4 (&buf)[kChunkVecs]) {
   constexpr int VEC = Chunk<DT>::kVec, ES = Chunk<DT>::kEs;
   const int lane = lane_id();
@@ -107,16 +124,40 @@ __device__ __forceinline__ void chunk_issue_t(const ChunkRef &r, uint4 (&buf)[kC
 #pragma unroll
   for (int u = 0; u < kChunkVecs; ++u) {
     const int e = (lane + 32 * u) * VEC;
-    if (e < r.n) buf[u] = ld_nc16(static_cast<const char *>(r.src) + (size_t)e * ES);
-    else buf[u] = make_uint4(ni, ni, ni, ni);
+    if (e < r.n && (!UNAL || e + VEC > r.lo))
+      buf[u] = ld_nc16(static_cast<const char *>(r.src) + (ptrdiff_t)e * ES);
+    else
+      buf[u] = make_uint4(ni, ni, ni, ni);
   }
 }
 
-template <int TDT, int DDT>
+template <int TDT, int DDT, bool UNAL>
 __device__ __forceinline__ void chunk_issue(const ChunkRef &r, uint4 (&buf)[kChunkVecs]) {
   if (r.kind == CK_SKIP) return;
-  if (TDT == DDT || !r.draft) chunk_issue_t<TDT>(r, buf);
-  else chunk_issue_t<DDT>(r, buf);
+  if (TDT == DDT || !r.draft) chunk_issue_t<TDT, UNAL>(r, buf);
+  else chunk_issue_t<DDT, UNAL>(r, buf);
+}
+
+// The vector of slots e .. e + VEC - 1 with the slots outside [lo, hi) set
+// to -inf.
+template <int DT>
+__device__ __forceinline__ uint4 mask_vec(uint4 v, int e, int lo, int hi) {
+  unsigned w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (DT == SV_F32) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (!(e + i >= lo && e + i < hi)) w[i] = 0xff800000u;
+  } else {
+    const unsigned ni = DT == SV_BF16 ? 0xff80u : 0xfc00u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int x = e + 2 * i;
+      const unsigned a = (x >= lo && x < hi) ? (w[i] & 0xffffu) : ni;
+      const unsigned b = (x + 1 >= lo && x + 1 < hi) ? (w[i] & 0xffff0000u) : (ni << 16);
+      w[i] = a | b;
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // NaN-propagating max of two packed words (2 x bf16, 2 x f16 or 1 x f32).
@@ -145,11 +186,21 @@ template <int DT> __device__ __forceinline__ float packed_word_max(unsigned w) {
   }
 }
 
-template <int DT>
-__device__ __forceinline__ void chunk_reduce(const ChunkRef &r, const uint4 (&buf)[kChunkVecs]) {
+// Reduces a loaded chunk; slots outside the row are masked (rows off the
+// 16-byte grid only: on the aligned path a row ends on a vector boundary and
+// the vectors past it were filled with -inf).
+template <int DT, bool UNAL>
+__device__ __forceinline__ void chunk_reduce(const ChunkRef &r, uint4 (&buf)[kChunkVecs]) {
   using C = Chunk<DT>;
   constexpr int VEC = C::kVec;
   const int lane = lane_id();
+  if (UNAL && (r.lo > 0 || r.n < C::kElems)) {  // a row's first or last chunk
+#pragma unroll
+    for (int u = 0; u < kChunkVecs; ++u) {
+      const int e = (lane + 32 * u) * VEC;
+      if (e < r.lo || e + VEC > r.n) buf[u] = mask_vec<DT>(buf[u], e, r.lo, r.n);
+    }
+  }
   // chunk maximum on packed words
   unsigned mw[4] = {buf[0].x, buf[0].y, buf[0].z, buf[0].w};
 #pragma unroll
@@ -208,8 +259,10 @@ __device__ __forceinline__ void chunk_reduce(const ChunkRef &r, const uint4 (&bu
       float v[VEC];
       Elt<DT>::unpack(buf[u], v);
 #pragma unroll
-      for (int t = VEC - 1; t >= 0; --t)
-        if (v[t] == m) idx = (lane + 32 * u) * VEC + t;  // descending: keeps the lowest
+      for (int t = VEC - 1; t >= 0; --t) {
+        const int e = (lane + 32 * u) * VEC + t;
+        if (v[t] == m && (!UNAL || (e >= r.lo && e < r.n))) idx = e;  // descending: keeps the lowest
+      }
     }
     idx = warp_min_int(idx);
     out = make_float2(m, __int_as_float(idx == 0x7fffffff ? idx : r.x0 + idx));
@@ -217,11 +270,11 @@ __device__ __forceinline__ void chunk_reduce(const ChunkRef &r, const uint4 (&bu
   if (lane == 0) part_store(r.dst, out.x, out.y, r.tag);
 }
 
-template <int MODE, int TDT, int DDT, bool PROBS>
-__device__ __forceinline__ void chunk_process(const ChunkRef &r, const uint4 (&buf)[kChunkVecs]) {
+template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
+__device__ __forceinline__ void chunk_process(const ChunkRef &r, uint4 (&buf)[kChunkVecs]) {
   if (r.kind == CK_SKIP) return;
-  if (TDT == DDT || !r.draft) chunk_reduce<TDT>(r, buf);
-  else chunk_reduce<DDT>(r, buf);
+  if (TDT == DDT || !r.draft) chunk_reduce<TDT, UNAL>(r, buf);
+  else chunk_reduce<DDT, UNAL>(r, buf);
 }
 
 // Dynamic work claims: kClaimStripes counters, counter s handing out the
@@ -267,6 +320,8 @@ __device__ __forceinline__ unsigned claim_issue(const PassParams &P, const Claim
   return v;
 }
 
+// The chunk of a claim made on the warp's current stripe (the one claim in
+// flight is always resolved before the warp can move to another stripe).
 __device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, unsigned pend,
                                              unsigned long long E) {
   const int lane = lane_id();
@@ -290,7 +345,7 @@ __device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, un
   return (int)k;
 }
 
-template <int MODE, int TDT, int DDT, bool PROBS>
+template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
 __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassParams P) {
   // The decide kernel may launch at once: its CTAs take the place of
   // finished stats CTAs and wait on the device for this grid to complete.
@@ -322,8 +377,8 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
   uint4 b0[kChunkVecs], b1[kChunkVecs];
   int ka = claim_resolve(P, cl, claim_issue(P, cl), E);
   if (ka >= 0) {
-    ChunkRef ra = decode_chunk<MODE, TDT, DDT, PROBS>(P, ka);
-    chunk_issue<TDT, DDT>(ra, b0);
+    ChunkRef ra = decode_chunk<MODE, TDT, DDT, PROBS, UNAL>(P, ka);
+    chunk_issue<TDT, DDT, UNAL>(ra, b0);
     unsigned pend = claim_issue(P, cl);  // the next claim is in flight while a chunk is reduced
     // two chunks per iteration so both buffers have static names
     while (true) {
@@ -331,19 +386,19 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
       ChunkRef rb;
       rb.kind = CK_SKIP;
       if (kb >= 0) {
-        rb = decode_chunk<MODE, TDT, DDT, PROBS>(P, kb);
-        chunk_issue<TDT, DDT>(rb, b1);
+        rb = decode_chunk<MODE, TDT, DDT, PROBS, UNAL>(P, kb);
+        chunk_issue<TDT, DDT, UNAL>(rb, b1);
         pend = claim_issue(P, cl);
       }
-      chunk_process<MODE, TDT, DDT, PROBS>(ra, b0);
+      chunk_process<MODE, TDT, DDT, PROBS, UNAL>(ra, b0);
       if (kb < 0) break;
       ka = claim_resolve(P, cl, pend, E);
       if (ka >= 0) {
-        ra = decode_chunk<MODE, TDT, DDT, PROBS>(P, ka);
-        chunk_issue<TDT, DDT>(ra, b0);
+        ra = decode_chunk<MODE, TDT, DDT, PROBS, UNAL>(P, ka);
+        chunk_issue<TDT, DDT, UNAL>(ra, b0);
         pend = claim_issue(P, cl);
       }
-      chunk_process<MODE, TDT, DDT, PROBS>(rb, b1);
+      chunk_process<MODE, TDT, DDT, PROBS, UNAL>(rb, b1);
       if (ka < 0) break;
     }
   }

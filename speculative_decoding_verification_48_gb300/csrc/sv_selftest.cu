@@ -7,7 +7,8 @@
 namespace sv {
 
 // scratch: 8 zeroed 64-bit words.  [0] the counter-reset "ready" word,
-// [1] the call's error word, [2] a decision flag.  None is ever set here.
+// [1] the call's error word, [2..5] two chunk partials that carry no call's
+// tag.  None is ever set here.
 __global__ void sv_wait_selftest_kernel(int which, unsigned long long *scratch,
                                         int32_t *out_status) {
   if (threadIdx.x >= 32) return;
@@ -21,9 +22,14 @@ __global__ void sv_wait_selftest_kernel(int which, unsigned long long *scratch,
       const bool flagged = __ldcg(scratch + 1) == E;
       *out_status = ok ? SV_ROW_OK : (flagged ? SV_ROW_TIMEOUT : SV_ROW_NONFINITE);
     }
-  } else if (threadIdx.x == 0) {
-    const unsigned f = wait_flag_bounded(reinterpret_cast<const unsigned *>(scratch + 2));
-    *out_status = f ? SV_ROW_OK : SV_ROW_TIMEOUT;
+  } else {
+    // the decide kernel's poll of a row's partials, on partials that never
+    // carry the awaited tag: it gives up after kPollSpins rounds (the decide
+    // kernel then takes the dependency wait)
+    float2 za, zb;
+    const bool ok = warp_rows_softmax2_poll(reinterpret_cast<const Part *>(scratch + 2), 2,
+                                            nullptr, 0, 1.f, 1u, kPollSpins, za, zb);
+    if (lane_id() == 0) *out_status = ok ? SV_ROW_OK : SV_ROW_TIMEOUT;
   }
 }
 

@@ -29,7 +29,8 @@ def test_header_declares_the_entry_points():
     for n in ("spec_verify_chain", "spec_verify_chain_greedy", "spec_verify_tree_greedy",
               "spec_verify_workspace_bytes", "spec_verify_status_string", "spec_draft_sample",
               "spec_tree_mask", "spec_tree_kv_compact", "spec_verify_chain_no_alloc",
-              "spec_verify_wait_selftest", "spec_verify_set_call_counter"):
+              "spec_verify_wait_selftest", "spec_verify_set_call_counter",
+              "spec_verify_force_stream_path"):
         assert n in names
 
 

@@ -118,7 +118,28 @@ def test_draft_sample_distribution_on_gpu(sv):
     assert stats.chisquare(obs, exp * (obs.sum() / exp.sum())).pvalue > 1e-3
 
 
-def test_draft_sample_rejects_unaligned_rows(sv):
-    case = W.make_draft("draft_odd", 5200, 2, 1001, "bf16")
-    with pytest.raises(sv.SpecVerifyError):
-        _run(sv, case)
+@pytest.mark.parametrize("dtype,V", [("bf16", 1001), ("f16", 70001), ("f32", 4099), ("bf16", 3)])
+def test_draft_sample_unaligned_rows(sv, dtype, V):
+    """Rows that do not start on 16-byte boundaries (odd V in 16-bit types,
+    V not a multiple of 4 in fp32): each row's chunks sit on the row's own
+    16-byte grid and its edge vectors are read element by element.  Greedy
+    and tiny-T rows included."""
+    case = W.make_draft(f"draft_odd_{dtype}_{V}", 5200 + V % 97, 13, V, dtype,
+                        temperature=_temps)
+    _check(sv, case)
+
+
+def test_draft_sample_unaligned_view(sv):
+    """A view that starts 2 bytes into an allocation: every row is off the
+    16-byte grid, including the first."""
+    case = W.make_draft("draft_view", 5300, 9, 4096, "bf16", temperature=_temps)
+    buf = torch.empty(case.B * case.V + 1, dtype=torch.bfloat16, device=DEV)
+    view = buf[1:].view(case.B, case.V)
+    view.copy_(case.logits.to(DEV))
+    tok, prob, st = sv.spec_draft_sample(view, case.temperatures.to(DEV), case.uniforms.to(DEV))
+    torch.cuda.synchronize()
+    l, T, u = case.numpy64()
+    ref = oracle.draft_sample(l, T, u)
+    assert np.array_equal(st.cpu().numpy(), ref["status"])
+    greedy = T <= 0
+    assert np.array_equal(tok.cpu().numpy()[greedy], ref["tokens"][greedy])

@@ -206,6 +206,21 @@ def test_chain_unaligned_rows(sv, V, dtype):
     check_chain(sv, case)
 
 
+def test_c3_shape_unaligned_rows_full(sv):
+    """C3's shape with V = 128257: every bf16 row starts at an odd multiple
+    of 2 bytes from the 16-byte grid, target and draft rows alike."""
+    case = W.make_chain("c3_unaligned", 1003, 64, 7, 128257, "bf16", target="zipf",
+                        draft_sigma=(0.3, 2.0), temperature=W._c3_temperature)
+    cmp, ref, out = check_chain(sv, case)
+    assert ref["greedy"].sum() == 8 and len(set(out[1].tolist())) > 3
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_tree_unaligned_rows(sv, dtype):
+    check_tree(sv, W.make_tree(f"tree_odd_{dtype}", 4600, B=5, N=40, V=9001, max_depth=8,
+                               kmin=1, kmax=3, dtype=dtype, p_match=0.9))
+
+
 def test_chain_mixed_dtypes(sv):
     base = W.make_chain("mixed", 3300, B=10, gamma=4, V=9000, dtype="bf16",
                         draft_sigma=(0.3, 1.0), temperature=_temps_mix)

@@ -30,7 +30,7 @@ def sv():
     return pkg
 
 
-@pytest.mark.parametrize("which", [0, 1], ids=["counter_reset_wait", "decision_flag_wait"])
+@pytest.mark.parametrize("which", [0, 1], ids=["counter_reset_wait", "partial_tag_poll"])
 def test_bounded_wait_gives_up_and_reports(sv, which):
     torch.cuda.synchronize()
     t0 = time.perf_counter()
