@@ -31,6 +31,9 @@
 namespace sv {
 
 constexpr int kClusterMax = 8;        // portable cluster size
+constexpr int kClThreads = 512;       // chain CTAs: 16 warps, one per kept row at a time
+constexpr int kClWarps = kClThreads / 32;
+constexpr int kClParts = kClusterMax * kClWarps;  // draw parts of a cluster: at most 128
 constexpr int kClusterSmemMax = 96 * 1024;  // kept row slices per chain CTA
 
 struct ClusterParams {
@@ -226,12 +229,12 @@ struct ClusterDraw {
 };
 
 template <int MODE, int TDT, int DDT, bool PROBS>
-__global__ void __launch_bounds__(kPassThreads, 1) sv_cluster_chain_kernel(const ClusterParams P) {
+__global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const ClusterParams P) {
   extern __shared__ __align__(16) unsigned char cl_rows[];  // kept row slices
   __shared__ float2 cl_part[kMaxRows];  // this CTA's partial of each row
   __shared__ float rowM[kMaxRows], rowZ[kMaxRows];
   __shared__ int rowI[kMaxRows];
-  __shared__ float cl_w[2][kPassWarps];  // this CTA's per-warp draw weights
+  __shared__ float cl_w[2][kClWarps];  // this CTA's per-warp draw weights
   __shared__ int cl_j, cl_kind;
   __shared__ ResidCoef cl_rk;
   __shared__ ClusterDraw cl_draw;
@@ -254,8 +257,16 @@ __global__ void __launch_bounds__(kPassThreads, 1) sv_cluster_chain_kernel(const
   const TT *tgt = reinterpret_cast<const TT *>(P.target) + (size_t)b * G1 * V;
   const DTy *drf = MODE == MODE_CHAIN ? reinterpret_cast<const DTy *>(P.draft) + (size_t)b * g * V
                                       : nullptr;
+  // 1. this CTA's slices into shared memory (every thread takes part in
+  // every row, so every copy is in flight at once)
+  for (int k = 0; k < nkeep; ++k) {
+    unsigned char *dst = cl_rows + (size_t)k * P.rstride;
+    if (k < G1) slice_copy<TDT>(dst, tgt + (size_t)k * V + x_lo, n, threadIdx.x, kClThreads);
+    else slice_copy<DDT>(dst, drf + (size_t)(k - G1) * V + x_lo, n, threadIdx.x, kClThreads);
+  }
+  cp_async_commit();
   // 0. the draft tokens and the logits at them (one lane per position),
-  // issued before the slice copies so that their latency overlaps
+  // issued while the copies are in flight; used by the accept tests
   const bool act = warp == 0 && lane < g;
   int x = 0;
   bool tok_ok = false;
@@ -270,20 +281,12 @@ __global__ void __launch_bounds__(kPassThreads, 1) sv_cluster_chain_kernel(const
     }
   }
   const float ug = (!badT && !greedy) ? __ldg(P.unif + (size_t)b * G1 + g) : 0.f;
-  // 1. this CTA's slices into shared memory (every thread takes part in
-  // every row, so every copy is in flight at once)
-  for (int k = 0; k < nkeep; ++k) {
-    unsigned char *dst = cl_rows + (size_t)k * P.rstride;
-    if (k < G1) slice_copy<TDT>(dst, tgt + (size_t)k * V + x_lo, n, threadIdx.x, kPassThreads);
-    else slice_copy<DDT>(dst, drf + (size_t)(k - G1) * V + x_lo, n, threadIdx.x, kPassThreads);
-  }
-  cp_async_commit();
   cp_async_wait_all();
   __syncthreads();
   // 2. slice partials: softmax rows (argmax for greedy rows); probability
   // drafts need none
   const int npart = greedy ? G1 : (PROBS ? G1 : G1 + g);
-  for (int k = warp; k < npart; k += kPassWarps) {
+  for (int k = warp; k < npart; k += kClWarps) {
     const unsigned char *row = cl_rows + (size_t)k * P.rstride;
     float2 pt;
     if (greedy) pt = slice_argmax<TDT>(row, n, x_lo);
@@ -292,25 +295,33 @@ __global__ void __launch_bounds__(kPassThreads, 1) sv_cluster_chain_kernel(const
     if (lane == 0) cl_part[k] = pt;
   }
   cluster_sync();  // 1: every CTA's partials are written
-  // 3. merge every row over the cluster (lane q reads CTA q's partial)
-  for (int k = warp; k < npart; k += kPassWarps) {
+  // 3. merge every row over the cluster: lane l of a warp reads CTA l % CS's
+  // partial of row l / CS of the warp's group of 32 / CS rows (one DSMEM
+  // round trip per group), and the CS lanes of a row reduce by shuffles
+  const int rpw = 32 / (int)CS;
+  for (int k0 = warp * rpw; k0 < npart; k0 += kClWarps * rpw) {
+    const int k = k0 + lane / (int)CS, q = lane % (int)CS;
     float2 pt = make_float2(-CUDART_INF_F, greedy ? __int_as_float(0x7fffffff) : 0.f);
-    if (lane < (int)CS) pt = ld_dsmem_f2(dsmem_addr(&cl_part[k], lane));
+    if (k < npart) pt = ld_dsmem_f2(dsmem_addr(&cl_part[k], (unsigned)q));
+    float M = pt.x;
+    for (int o = 1; o < (int)CS; o <<= 1) M = max_nan(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (greedy) {
-      const bool nan = __any_sync(0xffffffffu, isnan(pt.x));
-      const float M = warp_max_nan(pt.x);
-      const int I = warp_min_int(pt.x == M ? __float_as_int(pt.y) : 0x7fffffff);
-      if (lane == 0) {
+      int nan = isnan(pt.x) ? 1 : 0;
+      int I = pt.x == M ? __float_as_int(pt.y) : 0x7fffffff;
+      for (int o = 1; o < (int)CS; o <<= 1) {
+        nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+        I = min(I, __shfl_xor_sync(0xffffffffu, I, o));
+      }
+      if (q == 0 && k < npart) {
         rowM[k] = nan ? CUDART_NAN_F : M;
         rowI[k] = I;
       }
     } else {
-      const float M = warp_max_nan(pt.x);
-      const float z = (pt.x == -CUDART_INF_F) ? 0.f : pt.y * ex2((pt.x - M) * c);
-      const float Z = warp_sum(z);
-      if (lane == 0) {
+      float z = (pt.x == -CUDART_INF_F) ? 0.f : pt.y * ex2((pt.x - M) * c);
+      for (int o = 1; o < (int)CS; o <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      if (q == 0 && k < npart) {
         rowM[k] = M;
-        rowZ[k] = Z;
+        rowZ[k] = z;
       }
     }
   }
@@ -389,7 +400,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) sv_cluster_chain_kernel(const
   // of it.  kind 0 (a rejected pair): the residual, and p_j for the case of
   // a residual without mass; kind 1 (every draft accepted): the bonus row.
   const int kind = cl_kind, j = cl_j;
-  const int PER = (n + kPassThreads - 1) / kPassThreads;
+  const int PER = (n + kClThreads - 1) / kClThreads;
   const int L = 32 * PER;
   const ResidCoef rk = cl_rk;
   const unsigned char *prow = cl_rows + (size_t)(kind == 1 ? g : j) * P.rstride;
@@ -416,60 +427,81 @@ __global__ void __launch_bounds__(kPassThreads, 1) sv_cluster_chain_kernel(const
   }
   cluster_sync();  // 2: every CTA's weights are written
   // 6. every CTA's warp 0 reads the cluster's part weights (in vocabulary
-  // order: CTA rank, then warp) and locates the crossing of u R
+  // order: CTA rank, then warp; lane l holds parts l, l + 32, l + 64 and
+  // l + 96) and locates the crossing of u R
   if (kind >= 0 && warp == 0) {
-    const int parts = (int)CS * kPassWarps;  // at most 64: two per lane
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-    if (lane < parts) {
-      const unsigned q0 = (unsigned)(lane / kPassWarps);
-      a0 = ld_dsmem_f32(dsmem_addr(&cl_w[0][lane % kPassWarps], q0));
-      b0 = ld_dsmem_f32(dsmem_addr(&cl_w[1][lane % kPassWarps], q0));
+    constexpr int G = kClParts / 32;
+    const int parts = (int)CS * kClWarps;
+    float a[G], w[G];
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      const int pt = lane + 32 * i;
+      a[i] = w[i] = 0.f;
+      if (pt < parts) {
+        const unsigned q = (unsigned)(pt / kClWarps);
+        a[i] = ld_dsmem_f32(dsmem_addr(&cl_w[0][pt % kClWarps], q));
+        w[i] = ld_dsmem_f32(dsmem_addr(&cl_w[1][pt % kClWarps], q));
+      }
     }
-    if (lane + 32 < parts) {
-      const unsigned q1 = (unsigned)((lane + 32) / kPassWarps);
-      a1 = ld_dsmem_f32(dsmem_addr(&cl_w[0][(lane + 32) % kPassWarps], q1));
-      b1 = ld_dsmem_f32(dsmem_addr(&cl_w[1][(lane + 32) % kPassWarps], q1));
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < G; ++i) {
+      s0 += a[i];
+      s1 += w[i];
     }
-    const float R0 = warp_sum(a0 + a1), R1 = warp_sum(b0 + b1);
+    const float R0 = warp_sum(s0), R1 = warp_sum(s1);
     ClusterDraw d;
     d.R = R0;
     d.alt = kind == 0 && !isnan(R0) && !isinf(R0) && !(R0 > 0.f);
     const float R = d.alt ? R1 : R0;
-    const float w0 = d.alt ? b0 : a0, w1 = d.alt ? b1 : a1;
+    if (!d.alt) {
+#pragma unroll
+      for (int i = 0; i < G; ++i) w[i] = a[i];
+    }
     d.bad = isnan(R) || isinf(R) || !(R > 0.f);
     d.part = -1;
     d.base = 0.f;
     d.target = ug * R;
     if (!d.bad) {
-      float incl0 = w0, incl1 = w1;
+      // inclusive prefix over the parts in order, group by group
+      float incl[G], carry = 0.f;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y0 = __shfl_up_sync(0xffffffffu, incl0, o);
-        const float y1 = __shfl_up_sync(0xffffffffu, incl1, o);
-        if (lane >= o) {
-          incl0 += y0;
-          incl1 += y1;
+      for (int i = 0; i < G; ++i) {
+        float v = w[i];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += y;
+        }
+        incl[i] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+      int found = -1, lastpos = -1;
+      float base_found = 0.f, base_last = 0.f;
+#pragma unroll
+      for (int i = 0; i < G; ++i) {
+        const bool in = lane + 32 * i < parts;
+        const unsigned h = __ballot_sync(0xffffffffu, in && incl[i] > d.target);
+        const float before = __shfl_sync(0xffffffffu, incl[i] - w[i], h ? __ffs(h) - 1 : 0);
+        if (found < 0 && h) {
+          found = 32 * i + __ffs(h) - 1;
+          base_found = before;
+        }
+        const unsigned pm = __ballot_sync(0xffffffffu, in && w[i] > 0.f);
+        const float lb = __shfl_sync(0xffffffffu, incl[i] - w[i], pm ? 31 - __clz(pm) : 0);
+        if (pm) {
+          lastpos = 32 * i + 31 - __clz(pm);
+          base_last = lb;
         }
       }
-      incl1 += __shfl_sync(0xffffffffu, incl0, 31);
-      const unsigned h0 = __ballot_sync(0xffffffffu, lane < parts && incl0 > d.target);
-      const unsigned h1 = __ballot_sync(0xffffffffu, lane + 32 < parts && incl1 > d.target);
-      if (h0 || h1) {
-        const int l = h0 ? __ffs(h0) - 1 : __ffs(h1) - 1;
-        const float b0x = __shfl_sync(0xffffffffu, incl0 - w0, l);
-        const float b1x = __shfl_sync(0xffffffffu, incl1 - w1, l);
-        d.part = h0 ? l : 32 + l;
-        d.base = h0 ? b0x : b1x;
+      if (found >= 0) {
+        d.part = found;
+        d.base = base_found;
       } else {
         // rounding left no crossing: the last element of positive weight,
         // in the last part that holds one
-        const unsigned p0 = __ballot_sync(0xffffffffu, lane < parts && w0 > 0.f);
-        const unsigned p1 = __ballot_sync(0xffffffffu, lane + 32 < parts && w1 > 0.f);
-        const int l = p1 ? 31 - __clz(p1) : 31 - __clz(p0);
-        const float b0x = __shfl_sync(0xffffffffu, incl0 - w0, l);
-        const float b1x = __shfl_sync(0xffffffffu, incl1 - w1, l);
-        d.part = p1 ? 32 + l : l;
-        d.base = p1 ? b1x : b0x;
+        d.part = lastpos;
+        d.base = base_last;
         d.target = CUDART_INF_F;
       }
     }
@@ -479,7 +511,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) sv_cluster_chain_kernel(const
   __syncthreads();
   // 7. the part's owner rescans it from shared memory and writes the row
   const ClusterDraw d = cl_draw;
-  if (kind >= 0 && !d.bad && d.part / kPassWarps == (int)rank && warp == d.part % kPassWarps) {
+  if (kind >= 0 && !d.bad && d.part / kClWarps == (int)rank && warp == d.part % kClWarps) {
     const bool resid = kind == 0 && !d.alt;
     float tsum = 0.f;
     int lastpos = -1;

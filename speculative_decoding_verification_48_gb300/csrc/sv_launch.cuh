@@ -224,7 +224,7 @@ int cluster_capacity(int dev, int slot) {
     a[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(1u << slot);
-    cfg.blockDim = dim3(kPassThreads);
+    cfg.blockDim = dim3(MODE == MODE_TREE ? kPassThreads : kClThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = a;
     cfg.numAttrs = 1;
@@ -304,7 +304,7 @@ sv_status launch_cluster(const KParams &P0, const ClusterPlan &cp, cudaStream_t 
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)(P0.B * cp.CS));
-  cfg.blockDim = dim3(kPassThreads);
+  cfg.blockDim = dim3(MODE == MODE_TREE ? kPassThreads : kClThreads);
   cfg.dynamicSmemBytes = cp.smem;
   cfg.stream = stream;
   cfg.attrs = attr;

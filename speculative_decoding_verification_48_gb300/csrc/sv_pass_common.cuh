@@ -1,12 +1,13 @@
-// Shared definitions of the two-launch verification path: chunk geometry,
-// parameters, workspace layout, vector loads and warp-level merge /
+// Shared definitions of the two-launch (streaming) verification path: chunk
+// geometry, parameters, workspace layout, vector loads and warp-level merge /
 // crossing helpers.
 //
 //   sv_stats_kernel   streams every logit row once.  Each warp reduces
 //                     "warp-chunks" of 4 KB (32 lanes x 8 x 16-byte vectors)
 //                     to a partial — (max, sum exp2) for a softmax row,
 //                     (max, first index) for an argmax row — and stores it.
-//                     Warps are independent: no block barrier, no atomics.
+//                     Warps take chunks from striped claim counters (one
+//                     atomic per chunk) and take no block barrier.
 //   sv_decide_kernel  launched as a programmatic dependent of the first:
 //                     merges the partials of each batch row, runs the accept
 //                     tests / greedy match / tree walk, draws the bonus token

@@ -255,208 +255,394 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     }
     return;
   }
-  // 4. residual sweep of the row pair (p_j, q_j), chunks [c0, c1) of this CTA.
-  // Chunk ch covers vocabulary indices [ch kElems - off, (ch + 1) kElems -
-  // off), off being the target row's elements before its first vector
-  // boundary (0 when rows start on 16-byte boundaries), so the target row's
-  // vectors are aligned; the draft row's are too when its own offset agrees,
-  // else its elements are read one at a time.  Slots outside the row are
-  // masked: p = 0 there, so they add no mass.
-  using PC = PairChunk<TDT, DDT>;
-  using RA = RawVec<TDT, PC::kVec>;
-  using RQ = RawVec<DDT, PC::kVec>;
-  ResidCoef rk;
-  rk.c = c;
-  rk.Mp = sm.rowM[j];
-  rk.lzp = log2f(sm.rowZ[j]);
-  rk.Mq = PROBS ? 0.f : sm.rowM[G1 + j];
-  rk.lzq = PROBS ? 0.f : log2f(sm.rowZ[G1 + j]);
-  const float Mp = sm.rowM[j];
-  const TT *prow = tgt + (size_t)j * V;
-  const DTy *qrow = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V;
-  const int off = UNAL ? (int)((reinterpret_cast<uintptr_t>(prow) & (RA::kB - 1)) / sizeof(TT))
-                       : 0;
-  const bool qa = !UNAL || (reinterpret_cast<uintptr_t>(qrow - off) & (RQ::kB - 1)) == 0;
-  const unsigned padq = PROBS ? 0u : neg_inf_word<DDT>();
-  float *rs = P.resid + (size_t)b * P.cR;
-  const int c0 = (int)((long long)h * P.cR / P.H), c1 = (int)((long long)(h + 1) * P.cR / P.H);
-  // Each warp takes chunk pairs (ch, ch + 8), ch = c0 + warp + 16 i: the
-  // first chunk is loaded into registers, the second is copied into this
-  // warp's shared-memory stage by cp.async, and both are in flight before the
-  // first residual term (one memory round trip per pair).  Every lane reads
-  // back only the vectors it copied itself, so its own wait suffices.
-  typename RA::R *sa = reinterpret_cast<typename RA::R *>(sm.stage[warp]);
-  typename RQ::R *sq = reinterpret_cast<typename RQ::R *>(sm.stage[warp] + kResidBytes);
-  RA ra[PC::kVecs];
-  RQ rq[PC::kVecs];
-  auto chunk_sum = [&](int x0) {
-    unsigned long long s2 = 0ull;  // (+0, +0)
-#pragma unroll
-    for (int u = 0; u < PC::kVecs; ++u) {
-      const int x = x0 + (lane + 32 * u) * PC::kVec;
-      if (x < V && (!UNAL || x + PC::kVec > 0)) {
-        float a[PC::kVec], q[PC::kVec];
-        ra[u].unpack(a);
-        rq[u].unpack(q);
-        if (UNAL && (x < 0 || x + PC::kVec > V)) {
-#pragma unroll
-          for (int t = 0; t < PC::kVec; ++t)
-            if (x + t < 0 || x + t >= V) {
-              a[t] = -CUDART_INF_F;  // p = 0: no mass
-              q[t] = PROBS ? 0.f : -CUDART_INF_F;  // a neighbour's NaN stays out
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < PC::kVec; t += 2) {
-          const float2 r = resid_pair<PROBS>(a[t], a[t + 1], q[t], q[t + 1], rk);
-          s2 = f2_add(s2, f2_pack(r.x, r.y));
-        }
-      }
-    }
-    const float2 sp = f2_unpack(s2);
-    return warp_sum(sp.x + sp.y);
-  };
-  // 8-byte vectors (a 16-bit target beside fp32 draft rows) measured slower
-  // staged than one register-held chunk at a time, so only pairs of 16-byte
-  // vectors take the stage, and only when both rows' vectors are aligned
-  const bool stage = RA::kB == 16 && RQ::kB == 16 && qa;
-  const int stride = (stage ? 2 : 1) * kPassWarps;
-  for (int ch = c0 + warp; ch < c1; ch += stride) {
-    const int chB = ch + kPassWarps;
-    const bool useB = stage && chB < c1;
-    if (useB) {
-      const int xB = chB * PC::kElems - off;
-#pragma unroll
+  // 4-5.  Rows on the 16-byte grid take the first form (no offsets, no
+  // masks); rows off it the second.
+  if constexpr (!UNAL) {
+    // 4. residual sweep of the row pair (p_j, q_j), chunks [c0, c1) of this CTA
+    using PC = PairChunk<TDT, DDT>;
+    ResidCoef rk;
+    rk.c = c;
+    rk.Mp = sm.rowM[j];
+    rk.lzp = log2f(sm.rowZ[j]);
+    rk.Mq = PROBS ? 0.f : sm.rowM[G1 + j];
+    rk.lzq = PROBS ? 0.f : log2f(sm.rowZ[G1 + j]);
+    const float Mp = sm.rowM[j];
+    const TT *prow = tgt + (size_t)j * V;
+    const DTy *qrow = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V;
+    float *rs = P.resid + (size_t)b * P.cR;
+    const int c0 = (int)((long long)h * P.cR / P.H), c1 = (int)((long long)(h + 1) * P.cR / P.H);
+    // Each warp takes chunk pairs (ch, ch + 8), ch = c0 + warp + 16 i: the
+    // first chunk is loaded into registers, the second is copied into this
+    // warp's shared-memory stage by cp.async, and both are in flight before the
+    // first residual term (one memory round trip per pair).  Every lane reads
+    // back only the vectors it copied itself, so its own wait suffices.
+    using RA = RawVec<TDT, PC::kVec>;
+    using RQ = RawVec<DDT, PC::kVec>;
+    typename RA::R *sa = reinterpret_cast<typename RA::R *>(sm.stage[warp]);
+    typename RQ::R *sq = reinterpret_cast<typename RQ::R *>(sm.stage[warp] + kResidBytes);
+    RA ra[PC::kVecs];
+    RQ rq[PC::kVecs];
+    auto chunk_sum = [&](int n) {
+      unsigned long long s2 = 0ull;  // (+0, +0)
+  #pragma unroll
       for (int u = 0; u < PC::kVecs; ++u) {
-        const int x = xB + (lane + 32 * u) * PC::kVec;
-        if (x < V && (!UNAL || x + PC::kVec > 0)) {
-          cp_async<RA::kB>(sa + lane + 32 * u, prow + x);
-          cp_async<RQ::kB>(sq + lane + 32 * u, qrow + x);
+        const int e = (lane + 32 * u) * PC::kVec;
+        if (e < n) {
+          float a[PC::kVec], q[PC::kVec];
+          ra[u].unpack(a);
+          rq[u].unpack(q);
+  #pragma unroll
+          for (int t = 0; t < PC::kVec; t += 2) {
+            const float2 r = resid_pair<PROBS>(a[t], a[t + 1], q[t], q[t + 1], rk);
+            s2 = f2_add(s2, f2_pack(r.x, r.y));
+          }
         }
       }
-      cp_async_commit();
-    }
-    const int x0 = ch * PC::kElems - off;
-#pragma unroll
-    for (int u = 0; u < PC::kVecs; ++u) {
-      const int x = x0 + (lane + 32 * u) * PC::kVec;
-      if (x < V && (!UNAL || x + PC::kVec > 0)) {
-        ra[u].load(prow + x);
-        if (qa) rq[u].load(qrow + x);
-        else rq[u].r = raw_elements<DDT, PC::kVec>(qrow, x, V, padq);
+      const float2 sp = f2_unpack(s2);
+      return warp_sum(sp.x + sp.y);
+    };
+    // 8-byte vectors (a 16-bit target beside fp32 draft rows) measured slower
+    // staged than one register-held chunk at a time, so only pairs of 16-byte
+    // vectors take the stage
+    constexpr bool kStage = RA::kB == 16 && RQ::kB == 16;
+    for (int ch = c0 + warp; ch < c1; ch += (kStage ? 2 : 1) * kPassWarps) {
+      const int chB = ch + kPassWarps;
+      const int nB = kStage && chB < c1 ? min(PC::kElems, V - chB * PC::kElems) : 0;
+      if (nB > 0) {
+        const int xB = chB * PC::kElems;
+  #pragma unroll
+        for (int u = 0; u < PC::kVecs; ++u) {
+          const int e = (lane + 32 * u) * PC::kVec;
+          if (e < nB) {
+            cp_async<RA::kB>(sa + lane + 32 * u, prow + xB + e);
+            cp_async<RQ::kB>(sq + lane + 32 * u, qrow + xB + e);
+          }
+        }
+        cp_async_commit();
       }
-    }
-    const float s = chunk_sum(x0);
-    if (lane == 0) rs[ch] = s;
-    if (useB) {
-      cp_async_wait_all();
-      const int xB = chB * PC::kElems - off;
-#pragma unroll
+      const int x0 = ch * PC::kElems;
+      const int n = min(PC::kElems, V - x0);
+  #pragma unroll
       for (int u = 0; u < PC::kVecs; ++u) {
-        const int x = xB + (lane + 32 * u) * PC::kVec;
-        if (x < V && (!UNAL || x + PC::kVec > 0)) {
-          ra[u].r = sa[lane + 32 * u];
-          rq[u].r = sq[lane + 32 * u];
+        const int e = (lane + 32 * u) * PC::kVec;
+        if (e < n) {
+          ra[u].load(prow + x0 + e);
+          rq[u].load(qrow + x0 + e);
         }
       }
-      const float sB = chunk_sum(xB);
-      if (lane == 0) rs[chB] = sB;
+      const float s = chunk_sum(n);
+      if (lane == 0) rs[ch] = s;
+      if (nB > 0) {
+        cp_async_wait_all();
+  #pragma unroll
+        for (int u = 0; u < PC::kVecs; ++u) {
+          if ((lane + 32 * u) * PC::kVec < nB) {
+            ra[u].r = sa[lane + 32 * u];
+            rq[u].r = sq[lane + 32 * u];
+          }
+        }
+        const float sB = chunk_sum(nB);
+        if (lane == 0) rs[chB] = sB;
+      }
     }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    // a block that merged by polling waits here: the stats kernel zeroes
-    // done[] before its first partial, and the stats grid has long finished
-    // by now, so this returns at once
-    if (polled) grid_dependency_wait();
-    // one acquire-release add: it publishes this CTA's chunk sums (ordered
-    // before it by the barrier above) and, in the last CTA, acquires the
-    // other CTAs' sums
-    unsigned prev;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
-                 : "=r"(prev) : "l"(P.done + b) : "memory");
-    sm.last = (prev == (unsigned)P.H - 1u);
-  }
-  __syncthreads();
-  if (!sm.last) return;
-  // 5. the last CTA.  Every warp locates the crossing chunk of u * R from
-  // the same chunk sums; the chunk is rescanned by all eight warps, each
-  // over its eighth, and a prefix over the eight shares picks the warp that
-  // holds the crossing.  Warp 0, whose lanes hold the draft tokens, writes
-  // the row's outputs.
-  const float u = ug;
-  float R = 0.f, base = 0.f;
-  const int t = warp_chunk_cross(P.cR, [&](int k) { return __ldcg(rs + k); }, u, R, base);
-  if (isnan(R) || isinf(R) || !(R > 0.f)) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // a block that merged by polling waits here: the stats kernel zeroes
+      // done[] before its first partial, and the stats grid has long finished
+      // by now, so this returns at once
+      if (polled) grid_dependency_wait();
+      // one acquire-release add: it publishes this CTA's chunk sums (ordered
+      // before it by the barrier above) and, in the last CTA, acquires the
+      // other CTAs' sums
+      unsigned prev;
+      asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                   : "=r"(prev) : "l"(P.done + b) : "memory");
+      sm.last = (prev == (unsigned)P.H - 1u);
+    }
+    __syncthreads();
+    if (!sm.last) return;
+    // 5. the last CTA.  Every warp locates the crossing chunk of u * R from
+    // the same chunk sums; the chunk is rescanned by all eight warps, each
+    // over its eighth, and a prefix over the eight shares picks the warp that
+    // holds the crossing.  Warp 0, whose lanes hold the draft tokens, writes
+    // the row's outputs.
+    const float u = ug;
+    float R = 0.f, base = 0.f;
+    const int t = warp_chunk_cross(P.cR, [&](int k) { return __ldcg(rs + k); }, u, R, base);
+    if (isnan(R) || isinf(R) || !(R > 0.f)) {
+      if (warp != 0) return;
+      if (!(R > 0.f) && !isnan(R)) {
+        // no residual mass (p_j == q_j up to rounding): draw from p_j
+        const int k = warp_sample_softmax_row<TDT>(prow, pb + (size_t)j * P.cMax, P.cT, V, Mp, c, u);
+        for (int s = lane; s < G1; s += 32)
+          ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
+        if (lane == 0) {
+          P.out_nacc[b] = j;
+          if (P.out_status) P.out_status[b] = 0;
+          if (P.out_diag) P.out_diag[((size_t)b * g + j) * 4 + 3] = R;
+        }
+      } else {
+        pass_error_row(P, b, SV_ROW_NONFINITE, G1, ot, nullptr);
+      }
+      return;
+    }
+    const float target = u * R;
+    constexpr int SUB = PC::kElems / kPassWarps, SPER = SUB / 32;
+    static_assert(SPER % 2 == 0, "pairs of elements per lane");
+    const int xs = t * PC::kElems + warp * SUB;
+    float a[SPER], qv[SPER];
+    lane_row_load<TDT, SPER>(prow, xs, V, -CUDART_INF_F, a);
+    lane_row_load<DDT, SPER>(qrow, xs, V, PROBS ? 0.f : -CUDART_INF_F, qv);
+    float ls = 0.f;
+    int lpos = -1;
+  #pragma unroll
+    for (int e = 0; e < SPER; e += 2) {
+      const float2 r = resid_pair<PROBS>(a[e], a[e + 1], qv[e], qv[e + 1], rk);
+      a[e] = r.x;
+      a[e + 1] = r.y;
+    }
+  #pragma unroll
+    for (int e = 0; e < SPER; ++e) {
+      ls += a[e];
+      if (a[e] > 0.f) lpos = lane * SPER + e;
+    }
+    const float wt = warp_sum(ls);
+    const int wl = warp_max_int(lpos);
+    if (lane == 0) {
+      sm.tot[warp] = wt;
+      sm.lastp[warp] = wl >= 0 ? xs + wl : -1;
+    }
+    __syncthreads();
+    float bw = base;
+    int hw = -1;
+    for (int w = 0; w < kPassWarps && hw < 0; ++w) {
+      if (bw + sm.tot[w] > target) hw = w;
+      else bw += sm.tot[w];
+    }
+    if (warp == hw) {
+      const int kl = warp_rescan<SPER>(a, bw, target);
+      if (lane == 0) sm.k = xs + kl;
+    } else if (hw < 0 && warp == 0 && lane == 0) {
+      // rounding left no crossing: the last element of positive mass
+      int kk = t * PC::kElems;
+      for (int w = 0; w < kPassWarps; ++w)
+        if (sm.lastp[w] >= 0) kk = sm.lastp[w];
+      sm.k = kk;
+    }
+    __syncthreads();
     if (warp != 0) return;
-    if (!(R > 0.f) && !isnan(R)) {
-      // no residual mass (p_j == q_j up to rounding): draw from p_j
-      const int k = warp_sample_softmax_row<TDT>(prow, pb + (size_t)j * P.cMax, P.cT, V, Mp, c, u,
-                                                 P.unaligned ? row_offset16<TDT>(prow) : 0);
-      for (int s = lane; s < G1; s += 32)
-        ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
-      if (lane == 0) {
-        P.out_nacc[b] = j;
-        if (P.out_status) P.out_status[b] = 0;
-        if (P.out_diag) P.out_diag[((size_t)b * g + j) * 4 + 3] = R;
-      }
-    } else {
-      pass_error_row(P, b, SV_ROW_NONFINITE, G1, ot, nullptr);
+    const int k = sm.k;
+    for (int s = lane; s < G1; s += 32)
+      ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
+    if (lane == 0) {
+      P.out_nacc[b] = j;
+      if (P.out_status) P.out_status[b] = 0;
+      if (P.out_diag) P.out_diag[((size_t)b * g + j) * 4 + 3] = R;
     }
-    return;
-  }
-  const float target = u * R;
-  constexpr int SUB = PC::kElems / kPassWarps, SPER = SUB / 32;
-  static_assert(SPER % 2 == 0, "pairs of elements per lane");
-  const int xs = t * PC::kElems - off + warp * SUB;
-  float a[SPER], qv[SPER];
-  lane_row_load<TDT, SPER>(prow, xs, V, -CUDART_INF_F, a);
-  lane_row_load<DDT, SPER>(qrow, xs, V, PROBS ? 0.f : -CUDART_INF_F, qv);
-  float ls = 0.f;
-  int lpos = -1;
-#pragma unroll
-  for (int e = 0; e < SPER; e += 2) {
-    const float2 r = resid_pair<PROBS>(a[e], a[e + 1], qv[e], qv[e + 1], rk);
-    a[e] = r.x;
-    a[e + 1] = r.y;
-  }
-#pragma unroll
-  for (int e = 0; e < SPER; ++e) {
-    ls += a[e];
-    if (a[e] > 0.f) lpos = lane * SPER + e;
-  }
-  const float wt = warp_sum(ls);
-  const int wl = warp_max_int(lpos);
-  if (lane == 0) {
-    sm.tot[warp] = wt;
-    sm.lastp[warp] = wl >= 0 ? xs + wl : -1;
-  }
-  __syncthreads();
-  float bw = base;
-  int hw = -1;
-  for (int w = 0; w < kPassWarps && hw < 0; ++w) {
-    if (bw + sm.tot[w] > target) hw = w;
-    else bw += sm.tot[w];
-  }
-  if (warp == hw) {
-    const int kl = warp_rescan<SPER>(a, bw, target);
-    if (lane == 0) sm.k = xs + kl;
-  } else if (hw < 0 && warp == 0 && lane == 0) {
-    // rounding left no crossing: the last element of positive mass
-    int kk = t * PC::kElems;
-    for (int w = 0; w < kPassWarps; ++w)
-      if (sm.lastp[w] >= 0) kk = sm.lastp[w];
-    sm.k = kk;
-  }
-  __syncthreads();
-  if (warp != 0) return;
-  const int k = sm.k;
-  for (int s = lane; s < G1; s += 32)
-    ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
-  if (lane == 0) {
-    P.out_nacc[b] = j;
-    if (P.out_status) P.out_status[b] = 0;
-    if (P.out_diag) P.out_diag[((size_t)b * g + j) * 4 + 3] = R;
+  } else {
+    // 4. residual sweep of the row pair (p_j, q_j), chunks [c0, c1) of this CTA.
+    // Chunk ch covers vocabulary indices [ch kElems - off, (ch + 1) kElems -
+    // off), off being the target row's elements before its first vector
+    // boundary (0 when rows start on 16-byte boundaries), so the target row's
+    // vectors are aligned; the draft row's are too when its own offset agrees,
+    // else its elements are read one at a time.  Slots outside the row are
+    // masked: p = 0 there, so they add no mass.
+    using PC = PairChunk<TDT, DDT>;
+    using RA = RawVec<TDT, PC::kVec>;
+    using RQ = RawVec<DDT, PC::kVec>;
+    ResidCoef rk;
+    rk.c = c;
+    rk.Mp = sm.rowM[j];
+    rk.lzp = log2f(sm.rowZ[j]);
+    rk.Mq = PROBS ? 0.f : sm.rowM[G1 + j];
+    rk.lzq = PROBS ? 0.f : log2f(sm.rowZ[G1 + j]);
+    const float Mp = sm.rowM[j];
+    const TT *prow = tgt + (size_t)j * V;
+    const DTy *qrow = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V;
+    const int off = UNAL ? (int)((reinterpret_cast<uintptr_t>(prow) & (RA::kB - 1)) / sizeof(TT))
+                         : 0;
+    const bool qa = !UNAL || (reinterpret_cast<uintptr_t>(qrow - off) & (RQ::kB - 1)) == 0;
+    const unsigned padq = PROBS ? 0u : neg_inf_word<DDT>();
+    float *rs = P.resid + (size_t)b * P.cR;
+    const int c0 = (int)((long long)h * P.cR / P.H), c1 = (int)((long long)(h + 1) * P.cR / P.H);
+    // Each warp takes chunk pairs (ch, ch + 8), ch = c0 + warp + 16 i: the
+    // first chunk is loaded into registers, the second is copied into this
+    // warp's shared-memory stage by cp.async, and both are in flight before the
+    // first residual term (one memory round trip per pair).  Every lane reads
+    // back only the vectors it copied itself, so its own wait suffices.
+    typename RA::R *sa = reinterpret_cast<typename RA::R *>(sm.stage[warp]);
+    typename RQ::R *sq = reinterpret_cast<typename RQ::R *>(sm.stage[warp] + kResidBytes);
+    RA ra[PC::kVecs];
+    RQ rq[PC::kVecs];
+    auto chunk_sum = [&](int x0) {
+      unsigned long long s2 = 0ull;  // (+0, +0)
+  #pragma unroll
+      for (int u = 0; u < PC::kVecs; ++u) {
+        const int x = x0 + (lane + 32 * u) * PC::kVec;
+        if (x < V && (!UNAL || x + PC::kVec > 0)) {
+          float a[PC::kVec], q[PC::kVec];
+          ra[u].unpack(a);
+          rq[u].unpack(q);
+          if (UNAL && (x < 0 || x + PC::kVec > V)) {
+  #pragma unroll
+            for (int t = 0; t < PC::kVec; ++t)
+              if (x + t < 0 || x + t >= V) {
+                a[t] = -CUDART_INF_F;  // p = 0: no mass
+                q[t] = PROBS ? 0.f : -CUDART_INF_F;  // a neighbour's NaN stays out
+              }
+          }
+  #pragma unroll
+          for (int t = 0; t < PC::kVec; t += 2) {
+            const float2 r = resid_pair<PROBS>(a[t], a[t + 1], q[t], q[t + 1], rk);
+            s2 = f2_add(s2, f2_pack(r.x, r.y));
+          }
+        }
+      }
+      const float2 sp = f2_unpack(s2);
+      return warp_sum(sp.x + sp.y);
+    };
+    // 8-byte vectors (a 16-bit target beside fp32 draft rows) measured slower
+    // staged than one register-held chunk at a time, so only pairs of 16-byte
+    // vectors take the stage, and only when both rows' vectors are aligned
+    const bool stage = RA::kB == 16 && RQ::kB == 16 && qa;
+    const int stride = (stage ? 2 : 1) * kPassWarps;
+    for (int ch = c0 + warp; ch < c1; ch += stride) {
+      const int chB = ch + kPassWarps;
+      const bool useB = stage && chB < c1;
+      if (useB) {
+        const int xB = chB * PC::kElems - off;
+  #pragma unroll
+        for (int u = 0; u < PC::kVecs; ++u) {
+          const int x = xB + (lane + 32 * u) * PC::kVec;
+          if (x < V && (!UNAL || x + PC::kVec > 0)) {
+            cp_async<RA::kB>(sa + lane + 32 * u, prow + x);
+            cp_async<RQ::kB>(sq + lane + 32 * u, qrow + x);
+          }
+        }
+        cp_async_commit();
+      }
+      const int x0 = ch * PC::kElems - off;
+  #pragma unroll
+      for (int u = 0; u < PC::kVecs; ++u) {
+        const int x = x0 + (lane + 32 * u) * PC::kVec;
+        if (x < V && (!UNAL || x + PC::kVec > 0)) {
+          ra[u].load(prow + x);
+          if (qa) rq[u].load(qrow + x);
+          else rq[u].r = raw_elements<DDT, PC::kVec>(qrow, x, V, padq);
+        }
+      }
+      const float s = chunk_sum(x0);
+      if (lane == 0) rs[ch] = s;
+      if (useB) {
+        cp_async_wait_all();
+        const int xB = chB * PC::kElems - off;
+  #pragma unroll
+        for (int u = 0; u < PC::kVecs; ++u) {
+          const int x = xB + (lane + 32 * u) * PC::kVec;
+          if (x < V && (!UNAL || x + PC::kVec > 0)) {
+            ra[u].r = sa[lane + 32 * u];
+            rq[u].r = sq[lane + 32 * u];
+          }
+        }
+        const float sB = chunk_sum(xB);
+        if (lane == 0) rs[chB] = sB;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // a block that merged by polling waits here: the stats kernel zeroes
+      // done[] before its first partial, and the stats grid has long finished
+      // by now, so this returns at once
+      if (polled) grid_dependency_wait();
+      // one acquire-release add: it publishes this CTA's chunk sums (ordered
+      // before it by the barrier above) and, in the last CTA, acquires the
+      // other CTAs' sums
+      unsigned prev;
+      asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                   : "=r"(prev) : "l"(P.done + b) : "memory");
+      sm.last = (prev == (unsigned)P.H - 1u);
+    }
+    __syncthreads();
+    if (!sm.last) return;
+    // 5. the last CTA.  Every warp locates the crossing chunk of u * R from
+    // the same chunk sums; the chunk is rescanned by all eight warps, each
+    // over its eighth, and a prefix over the eight shares picks the warp that
+    // holds the crossing.  Warp 0, whose lanes hold the draft tokens, writes
+    // the row's outputs.
+    const float u = ug;
+    float R = 0.f, base = 0.f;
+    const int t = warp_chunk_cross(P.cR, [&](int k) { return __ldcg(rs + k); }, u, R, base);
+    if (isnan(R) || isinf(R) || !(R > 0.f)) {
+      if (warp != 0) return;
+      if (!(R > 0.f) && !isnan(R)) {
+        // no residual mass (p_j == q_j up to rounding): draw from p_j
+        const int k = warp_sample_softmax_row<TDT>(prow, pb + (size_t)j * P.cMax, P.cT, V, Mp, c, u,
+                                                   P.unaligned ? row_offset16<TDT>(prow) : 0);
+        for (int s = lane; s < G1; s += 32)
+          ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
+        if (lane == 0) {
+          P.out_nacc[b] = j;
+          if (P.out_status) P.out_status[b] = 0;
+          if (P.out_diag) P.out_diag[((size_t)b * g + j) * 4 + 3] = R;
+        }
+      } else {
+        pass_error_row(P, b, SV_ROW_NONFINITE, G1, ot, nullptr);
+      }
+      return;
+    }
+    const float target = u * R;
+    constexpr int SUB = PC::kElems / kPassWarps, SPER = SUB / 32;
+    static_assert(SPER % 2 == 0, "pairs of elements per lane");
+    const int xs = t * PC::kElems - off + warp * SUB;
+    float a[SPER], qv[SPER];
+    lane_row_load<TDT, SPER>(prow, xs, V, -CUDART_INF_F, a);
+    lane_row_load<DDT, SPER>(qrow, xs, V, PROBS ? 0.f : -CUDART_INF_F, qv);
+    float ls = 0.f;
+    int lpos = -1;
+  #pragma unroll
+    for (int e = 0; e < SPER; e += 2) {
+      const float2 r = resid_pair<PROBS>(a[e], a[e + 1], qv[e], qv[e + 1], rk);
+      a[e] = r.x;
+      a[e + 1] = r.y;
+    }
+  #pragma unroll
+    for (int e = 0; e < SPER; ++e) {
+      ls += a[e];
+      if (a[e] > 0.f) lpos = lane * SPER + e;
+    }
+    const float wt = warp_sum(ls);
+    const int wl = warp_max_int(lpos);
+    if (lane == 0) {
+      sm.tot[warp] = wt;
+      sm.lastp[warp] = wl >= 0 ? xs + wl : -1;
+    }
+    __syncthreads();
+    float bw = base;
+    int hw = -1;
+    for (int w = 0; w < kPassWarps && hw < 0; ++w) {
+      if (bw + sm.tot[w] > target) hw = w;
+      else bw += sm.tot[w];
+    }
+    if (warp == hw) {
+      const int kl = warp_rescan<SPER>(a, bw, target);
+      if (lane == 0) sm.k = xs + kl;
+    } else if (hw < 0 && warp == 0 && lane == 0) {
+      // rounding left no crossing: the last element of positive mass
+      int kk = t * PC::kElems;
+      for (int w = 0; w < kPassWarps; ++w)
+        if (sm.lastp[w] >= 0) kk = sm.lastp[w];
+      sm.k = kk;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    const int k = sm.k;
+    for (int s = lane; s < G1; s += 32)
+      ot[s] = s < j ? x : (s == j ? k : -1);  // lane s holds draft token s
+    if (lane == 0) {
+      P.out_nacc[b] = j;
+      if (P.out_status) P.out_status[b] = 0;
+      if (P.out_diag) P.out_diag[((size_t)b * g + j) * 4 + 3] = R;
+    }
   }
 }
 
