@@ -54,9 +54,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["c3", "c5", "c2", "c1", "c4", "draft"], default="c3",
-                    help="c4 (token trees: mask, greedy walk, KV compaction) and draft (the "
-                         "draft-side sampler, 1024 rows x 128256 bf16) are accepted in --ncu "
+    ap.add_argument("--workload", choices=["c3", "c5", "c2", "c1", "c4", "draft", "c3u"],
+                    default="c3",
+                    help="c4 (token trees: mask, greedy walk, KV compaction), draft (the "
+                         "draft-side sampler, 1024 rows x 128256 bf16) and c3u (the C3 shape "
+                         "with V = 128257: rows off the 16-byte grid) are accepted in --ncu "
                          "mode only")
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -85,6 +87,10 @@ def make_workload(name: str, row0: int = 0):
     if name == "c2":
         return W.make_chain("c2_chain_B1_g5_V32000_bf16_T1.0", 1002, 1, 5, 32000, "bf16",
                             target="zipf", temperature=1.0, row0=row0)
+    if name == "c3u":
+        return W.make_chain("c3_unaligned_B64_g7_V128257_bf16", 1003, 64, 7, 128257, "bf16",
+                            target="zipf", draft_sigma=(0.3, 2.0),
+                            temperature=W._c3_temperature, row0=row0)
     if name == "c1":
         return W.make_chain("c1_chain_B1_g4_V1000_f32", 1001, 1, 4, 1000, "f32",
                             target="normal", target_sigma=2.0, draft_sigma=(0.5, 0.5),

@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
   __shared__ int rowI[kMaxRows];
   __shared__ float cl_w[2][kClWarps];  // this CTA's per-warp draw weights
   __shared__ int cl_j, cl_kind;
+  __shared__ int cl_x[32];  // the draft tokens, for the row's outputs
   __shared__ ResidCoef cl_rk;
   __shared__ ClusterDraw cl_draw;
   using TT = typename Elt<TDT>::T;
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
   float lp = 0.f, lq = 0.f, ui = 0.f;
   if (act && !badT) {
     x = __ldg(P.draft_tokens + (size_t)b * g + lane);
+    cl_x[lane] = x;
     tok_ok = x >= 0 && x < V;
     if (!greedy && tok_ok) {
       lp = Elt<TDT>::load1(tgt + (size_t)lane * V + x);
@@ -549,8 +551,7 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
     }
     k += x_lo;
     int32_t *ot = P.out_tokens + (size_t)b * G1;
-    const int32_t *xt = P.draft_tokens + (size_t)b * g;
-    for (int s = lane; s < G1; s += 32) ot[s] = s < j ? __ldg(xt + s) : (s == j ? k : -1);
+    for (int s = lane; s < G1; s += 32) ot[s] = s < j ? cl_x[s] : (s == j ? k : -1);
     if (lane == 0) {
       P.out_nacc[b] = j;
       if (P.out_status) P.out_status[b] = 0;

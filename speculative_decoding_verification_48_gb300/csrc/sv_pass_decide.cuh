@@ -24,7 +24,9 @@ struct DecideSmem {
   int lastp[kPassWarps];  // ... and its last index of positive mass (-1: none)
   int k;                  // the drawn token
   // per warp: the p and q halves of one residual chunk, copied in by cp.async
-  alignas(16) unsigned char stage[kPassWarps][2 * kResidBytes];
+  // (q may take one 16-byte block more: its vectors rebuilt from blocks of
+  // its own grid)
+  alignas(16) unsigned char stage[kPassWarps][2 * kResidBytes + 16];
 };
 
 struct TreeSmem {
@@ -49,31 +51,91 @@ static __device__ __noinline__ void pass_error_row(const PassParams &P, int b, i
   }
 }
 
-// Bits of one vector of VEC elements of a row at vocabulary index x, read
-// one element at a time: elements inside [0, V) are loaded, the others get
-// the bits `pad` (a packed element pattern).
-template <int DT, int VEC>
-__device__ __forceinline__ typename RawVec<DT, VEC>::R raw_elements(const typename Elt<DT>::T *row,
-                                                                    int x, int V, unsigned pad) {
-  typename RawVec<DT, VEC>::R r;
-  unsigned *w = reinterpret_cast<unsigned *>(&r);
-  constexpr int W = (int)(sizeof(r) / 4);
-  if constexpr (DT == SV_F32) {
+// The bytes [s, s + 16) of the 32-byte concatenation (lo, hi), s an even
+// byte offset below 16 (uniform across the warp).
+__device__ __forceinline__ uint4 bytes_at(const uint4 &lo, const uint4 &hi, int s) {
+  const unsigned c[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const unsigned r = (unsigned)(s & 3) * 8u;
+  unsigned o[4];
+  switch (s >> 2) {
+#define SV_BYTES_AT(W)                                                            \
+  case W:                                                                          \
+    _Pragma("unroll") for (int i = 0; i < 4; ++i)                                  \
+      o[i] = r ? __funnelshift_r(c[W + i], c[W + i + 1], r) : c[W + i];             \
+    break;
+    SV_BYTES_AT(0)
+    SV_BYTES_AT(1)
+    SV_BYTES_AT(2)
+    default:
+      _Pragma("unroll") for (int i = 0; i < 4; ++i)
+        o[i] = r ? __funnelshift_r(c[3 + i], c[3 + i + 1], r) : c[3 + i];
+      break;
+#undef SV_BYTES_AT
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+// The same for 8-byte vectors: bytes [s, s + 8) of (lo, hi), s even, < 8.
+__device__ __forceinline__ uint2 bytes_at(const uint2 &lo, const uint2 &hi, int s) {
+  const unsigned r = (unsigned)(s & 3) * 8u;
+  if (s < 4) return r ? make_uint2(__funnelshift_r(lo.x, lo.y, r), __funnelshift_r(lo.y, hi.x, r))
+                      : lo;
+  return r ? make_uint2(__funnelshift_r(lo.y, hi.x, r), __funnelshift_r(hi.x, hi.y, r))
+           : make_uint2(lo.y, hi.x);
+}
+__device__ __forceinline__ uint4 shfl_vec(const uint4 &v, int src) {
+  return make_uint4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
+                    __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
+}
+__device__ __forceinline__ uint2 shfl_vec(const uint2 &v, int src) {
+  return make_uint2(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src));
+}
+__device__ __forceinline__ uint4 shfl_down_vec(const uint4 &v) {
+  return make_uint4(__shfl_down_sync(0xffffffffu, v.x, 1), __shfl_down_sync(0xffffffffu, v.y, 1),
+                    __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
+}
+__device__ __forceinline__ uint2 shfl_down_vec(const uint2 &v) {
+  return make_uint2(__shfl_down_sync(0xffffffffu, v.x, 1), __shfl_down_sync(0xffffffffu, v.y, 1));
+}
+
+// The lanes' vectors of a row whose own vector grid is shifted by mq bytes
+// (0 < mq < the vector width) from the grid they are read on: vector i of
+// the warp (i = lane + 32 u) starts at byte `a0 + i * kB`.  Each lane loads
+// the aligned block under its vector's first byte; the block after it is the
+// next lane's (the next group's lane 0 for lane 31, and one more load after
+// the last group), so each vector costs one aligned load and two shuffles
+// of its words.  Blocks that hold no byte of [lo, hi) are not loaded (their
+// slots are masked by the caller).
+template <class R, int KVECS>
+__device__ __forceinline__ void load_realigned(const char *a0, int mq, const char *lo,
+                                               const char *hi, R (&out)[KVECS]) {
+  constexpr int kB = (int)sizeof(R);
+  const int lane = lane_id();
+  R blk[KVECS];
 #pragma unroll
-    for (int i = 0; i < W; ++i)
-      w[i] = (x + i >= 0 && x + i < V) ? __ldg(reinterpret_cast<const unsigned *>(row) + x + i)
-                                       : pad;
-  } else {
-    const unsigned short *h = reinterpret_cast<const unsigned short *>(row);
-#pragma unroll
-    for (int i = 0; i < W; ++i) {
-      const int xa = x + 2 * i, xb = xa + 1;
-      const unsigned a = (xa >= 0 && xa < V) ? __ldg(h + xa) : (pad & 0xffffu);
-      const unsigned bb = (xb >= 0 && xb < V) ? __ldg(h + xb) : (pad >> 16);
-      w[i] = a | (bb << 16);
+  for (int u = 0; u < KVECS; ++u) {
+    const char *bq = a0 + (ptrdiff_t)(lane + 32 * u) * kB - mq;
+    if (bq + kB > lo && bq < hi) {
+      if constexpr (kB == 16) blk[u] = ld_nc16(bq);
+      else blk[u] = ld_nc8(bq);
+    } else {
+      blk[u] = R{};
     }
   }
-  return r;
+  R ext = R{};
+  {
+    const char *bq = a0 + (ptrdiff_t)(32 * KVECS) * kB - mq;
+    if (lane == 31 && bq + kB > lo && bq < hi) {
+      if constexpr (kB == 16) ext = ld_nc16(bq);
+      else ext = ld_nc8(bq);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < KVECS; ++u) {
+    R nb = shfl_down_vec(blk[u]);
+    const R first_next = shfl_vec(u + 1 < KVECS ? blk[(u + 1) % KVECS] : ext, u + 1 < KVECS ? 0 : 31);
+    if (lane == 31) nb = first_next;
+    out[u] = bytes_at(blk[u], nb, mq);
+  }
 }
 
 // Chain rows.  Every CTA of the row merges the partials it needs and makes
@@ -461,8 +523,8 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     const DTy *qrow = reinterpret_cast<const DTy *>(P.draft) + ((size_t)b * g + j) * V;
     const int off = UNAL ? (int)((reinterpret_cast<uintptr_t>(prow) & (RA::kB - 1)) / sizeof(TT))
                          : 0;
-    const bool qa = !UNAL || (reinterpret_cast<uintptr_t>(qrow - off) & (RQ::kB - 1)) == 0;
-    const unsigned padq = PROBS ? 0u : neg_inf_word<DDT>();
+    const int mq = (int)(reinterpret_cast<uintptr_t>(qrow - off) & (RQ::kB - 1));  // bytes
+    const bool qa = !UNAL || mq == 0;
     float *rs = P.resid + (size_t)b * P.cR;
     const int c0 = (int)((long long)h * P.cR / P.H), c1 = (int)((long long)(h + 1) * P.cR / P.H);
     // Each warp takes chunk pairs (ch, ch + 8), ch = c0 + warp + 16 i: the
@@ -503,8 +565,8 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
     };
     // 8-byte vectors (a 16-bit target beside fp32 draft rows) measured slower
     // staged than one register-held chunk at a time, so only pairs of 16-byte
-    // vectors take the stage, and only when both rows' vectors are aligned
-    const bool stage = RA::kB == 16 && RQ::kB == 16 && qa;
+    // vectors take the stage
+    const bool stage = RA::kB == 16 && RQ::kB == 16;
     const int stride = (stage ? 2 : 1) * kPassWarps;
     for (int ch = c0 + warp; ch < c1; ch += stride) {
       const int chB = ch + kPassWarps;
@@ -516,32 +578,54 @@ __device__ void decide_chain_row(const PassParams &P, int b, int h, DecideSmem &
           const int x = xB + (lane + 32 * u) * PC::kVec;
           if (x < V && (!UNAL || x + PC::kVec > 0)) {
             cp_async<RA::kB>(sa + lane + 32 * u, prow + x);
-            cp_async<RQ::kB>(sq + lane + 32 * u, qrow + x);
+            if (qa) cp_async<RQ::kB>(sq + lane + 32 * u, qrow + x);
+          }
+        }
+        if (!qa) {
+          // the draft row's aligned blocks under the vectors, one more after
+          // them (blocks that hold no byte of the row are not copied: the
+          // slots they would fill are masked)
+          const char *q0 = reinterpret_cast<const char *>(qrow + xB) - mq;
+          const char *qlo = reinterpret_cast<const char *>(qrow);
+          const char *qhi = reinterpret_cast<const char *>(qrow + V);
+          for (int i = lane; i <= 32 * PC::kVecs; i += 32) {
+            const char *bq = q0 + (ptrdiff_t)i * RQ::kB;
+            if (bq + RQ::kB > qlo && bq < qhi) cp_async<RQ::kB>(sq + i, bq);
           }
         }
         cp_async_commit();
       }
       const int x0 = ch * PC::kElems - off;
+      if (!qa) {
+        // the draft row's vectors are shifted from the target row's grid
+        typename RQ::R qv[PC::kVecs];
+        load_realigned<typename RQ::R, PC::kVecs>(
+            reinterpret_cast<const char *>(qrow + x0), mq, reinterpret_cast<const char *>(qrow),
+            reinterpret_cast<const char *>(qrow + V), qv);
+  #pragma unroll
+        for (int u = 0; u < PC::kVecs; ++u) rq[u].r = qv[u];
+      }
   #pragma unroll
       for (int u = 0; u < PC::kVecs; ++u) {
         const int x = x0 + (lane + 32 * u) * PC::kVec;
         if (x < V && (!UNAL || x + PC::kVec > 0)) {
           ra[u].load(prow + x);
           if (qa) rq[u].load(qrow + x);
-          else rq[u].r = raw_elements<DDT, PC::kVec>(qrow, x, V, padq);
         }
       }
       const float s = chunk_sum(x0);
       if (lane == 0) rs[ch] = s;
       if (useB) {
         cp_async_wait_all();
+        if (!qa) __syncwarp();  // a vector's second block was copied by the next lane
         const int xB = chB * PC::kElems - off;
   #pragma unroll
         for (int u = 0; u < PC::kVecs; ++u) {
           const int x = xB + (lane + 32 * u) * PC::kVec;
           if (x < V && (!UNAL || x + PC::kVec > 0)) {
             ra[u].r = sa[lane + 32 * u];
-            rq[u].r = sq[lane + 32 * u];
+            rq[u].r = qa ? sq[lane + 32 * u]
+                         : bytes_at(sq[lane + 32 * u], sq[lane + 32 * u + 1], mq);
           }
         }
         const float sB = chunk_sum(xB);

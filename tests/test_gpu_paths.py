@@ -48,6 +48,20 @@ def test_mixed_dtypes(svp):
     TP.test_chain_mixed_dtypes(svp)
 
 
+@pytest.mark.parametrize("tdt,ddt", [("bf16", torch.float32), ("f32", torch.bfloat16),
+                                     ("bf16", torch.float16)])
+def test_mixed_dtypes_rows_off_grid(svp, tdt, ddt):
+    """Target and draft rows of different widths and odd V, so that the
+    rows start at shifting offsets from the 16-byte grid: on the streaming
+    path the draft row's vectors are rebuilt from aligned blocks of its own
+    grid (16- and 8-byte vectors)."""
+    base = W.make_chain(f"mixed_odd_{tdt}", 3400, B=9, gamma=4, V=9001, dtype=tdt,
+                        draft_sigma=(0.3, 1.0), temperature=TP._temps_mix)
+    case = W.ChainCase("mixed_odd", base.target, base.draft.to(ddt), False, base.draft_tokens,
+                       base.temperatures, base.uniforms, dict(dtype="bf16"))
+    TP.check_chain(svp, case)
+
+
 @pytest.mark.parametrize("gamma", [1, 31])
 def test_gamma_extremes(svp, gamma):
     TP.test_chain_gamma_extremes(svp, gamma)
