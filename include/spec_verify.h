@@ -276,9 +276,10 @@ SV_API sv_status spec_verify_wait_selftest(int which, void *scratch, int32_t *ou
                                            sv_stream_t stream);
 
 /*
- * Diagnostics.  Small calls (chains whose kept row slices fit one cluster of
- * at most 8 CTAs per batch row, trees of at most 1 MB of node-row slices per
- * CTA, in one wave) run on the cluster path: one launch, no workspace use.
+ * Diagnostics.  Small calls (chains whose kept row slices fit the shared
+ * memory of one cluster of at most 8 CTAs per batch row; trees of at most
+ * 1 MB of node-row slices per CTA; every cluster resident at once) run on
+ * the cluster path: one launch, no workspace use.
  * Every other call runs the two-launch streaming path.  With on != 0 every
  * call takes the streaming path (tests use this to check both paths on the
  * same shapes); returns the previous setting.  Process-wide.

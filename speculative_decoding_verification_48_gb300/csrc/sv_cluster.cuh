@@ -30,7 +30,7 @@
 
 namespace sv {
 
-constexpr int kClusterMax = 8;        // portable cluster size
+constexpr int kClusterMax = 8;        // largest cluster: the portable size
 constexpr int kClThreads = 512;       // chain CTAs: 16 warps, one per kept row at a time
 constexpr int kClWarps = kClThreads / 32;
 constexpr int kClParts = kClusterMax * kClWarps;  // draw parts of a cluster: at most 128
@@ -266,25 +266,28 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
     else slice_copy<DDT>(dst, drf + (size_t)(k - G1) * V + x_lo, n, threadIdx.x, kClThreads);
   }
   cp_async_commit();
-  // 0. the draft tokens and the logits at them (one lane per position),
-  // issued while the copies are in flight; used by the accept tests
+  // 0. the draft tokens and the uniforms (one lane per position), issued
+  // while the copies are in flight; the logits at the tokens are gathered
+  // after the copies (below), so no warp waits for the dependent load
   const bool act = warp == 0 && lane < g;
   int x = 0;
   bool tok_ok = false;
   float lp = 0.f, lq = 0.f, ui = 0.f;
   if (act && !badT) {
     x = __ldg(P.draft_tokens + (size_t)b * g + lane);
-    cl_x[lane] = x;
-    tok_ok = x >= 0 && x < V;
-    if (!greedy && tok_ok) {
-      lp = Elt<TDT>::load1(tgt + (size_t)lane * V + x);
-      lq = Elt<DDT>::load1(drf + (size_t)lane * V + x);
-      ui = __ldg(P.unif + (size_t)b * G1 + lane);
-    }
+    if (!greedy) ui = __ldg(P.unif + (size_t)b * G1 + lane);
   }
   const float ug = (!badT && !greedy) ? __ldg(P.unif + (size_t)b * G1 + g) : 0.f;
   cp_async_wait_all();
   __syncthreads();
+  if (act && !badT) {
+    cl_x[lane] = x;
+    tok_ok = x >= 0 && x < V;
+    if (!greedy && tok_ok) {  // used by the accept tests, after the row statistics
+      lp = Elt<TDT>::load1(tgt + (size_t)lane * V + x);
+      lq = Elt<DDT>::load1(drf + (size_t)lane * V + x);
+    }
+  }
   // 2. slice partials: softmax rows (argmax for greedy rows); probability
   // drafts need none
   const int npart = greedy ? G1 : (PROBS ? G1 : G1 + g);
@@ -429,8 +432,8 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
   }
   cluster_sync();  // 2: every CTA's weights are written
   // 6. every CTA's warp 0 reads the cluster's part weights (in vocabulary
-  // order: CTA rank, then warp; lane l holds parts l, l + 32, l + 64 and
-  // l + 96) and locates the crossing of u R
+  // order: CTA rank, then warp; lane l holds parts l, l + 32, l + 64, ...)
+  // and locates the crossing of u R
   if (kind >= 0 && warp == 0) {
     constexpr int G = kClParts / 32;
     const int parts = (int)CS * kClWarps;
@@ -558,7 +561,12 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
       if (P.out_diag && kind == 0) P.out_diag[((size_t)b * g + j) * 4 + 3] = d.R;
     }
   }
-  cluster_sync();  // 3: no CTA leaves while another may read its shared memory
+  // 3: no CTA leaves while another may read its shared memory.  Every DSMEM
+  // read of this kernel has returned its value before its warp arrives, so
+  // the arrival needs no release (the row's global writes need none either:
+  // the kernel's end makes them visible)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+               "barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // Trees: CTA r of tree b's cluster streams its slice of every node row.

@@ -195,7 +195,9 @@ struct ClusterPlan {
 };
 
 constexpr size_t kTreeUnitSmemMax = 16 * 1024;  // tree unit partials per CTA
-constexpr long long kClusterTreeBytesMax = 8LL << 20;  // node-row bytes of a cluster-path call
+constexpr long long kClusterTreeBytesMax = 8LL << 20;  // node-row bytes of a small tree call
+constexpr int kClusterSlots = 4;                       // cluster sizes 1, 2, 4, 8
+constexpr int kClusterMinSlice = 1024;                 // vocabulary entries per chain CTA
 
 template <int MODE, int TDT, int DDT, bool PROBS>
 void *cluster_kernel() {
@@ -206,10 +208,11 @@ void *cluster_kernel() {
 }
 
 // Clusters of CS CTAs (CS = 1, 2, 4, 8 -> slot 0..3) that fit on the device
-// at once; 0 if the kernel cannot be set up.
+// at once; 0 if the kernel cannot be set up.  (Clusters of 16, a
+// non-portable size, measured slower on the single-round chains.)
 template <int MODE, int TDT, int DDT, bool PROBS>
 int cluster_capacity(int dev, int slot) {
-  static std::atomic<int> cache[kMaxDevices][4];
+  static std::atomic<int> cache[kMaxDevices][kClusterSlots];
   int v = cache[dev][slot].load(std::memory_order_relaxed);
   if (v != 0) return v > 0 ? v : 0;
   const void *kern = cluster_kernel<MODE, TDT, DDT, PROBS>();
@@ -240,16 +243,18 @@ bool cluster_plan(const KParams &P, int dev, ClusterPlan &cp) {
   if (force_stream_path() || dev < 0 || dev >= kMaxDevices) return false;
   constexpr int esT = (TDT == SV_F32) ? 4 : 2, esD = (DDT == SV_F32) ? 4 : 2;
   if (MODE == MODE_TREE) {
-    // larger calls stream faster over every SM with the two-launch path
-    if (!rows_aligned(P.target, P.V, esT) || P.N > SV_MAX_TREE_NODES ||
-        (long long)P.B * P.N * P.V * esT > kClusterTreeBytesMax)
-      return false;
+    if (!rows_aligned(P.target, P.V, esT) || P.N > SV_MAX_TREE_NODES) return false;
+    // a large call takes the cluster path only when its clusters put a CTA
+    // on every SM; otherwise the streaming path's full grid reads faster
+    const bool small = (long long)P.B * P.N * P.V * esT <= kClusterTreeBytesMax;
+    const int sms = sm_count(dev);
     constexpr int E = Chunk<TDT>::kElems;
-    for (int slot = 3; slot >= 0; --slot) {
+    for (int slot = kClusterSlots - 1; slot >= 0; --slot) {
       const int CS = 1 << slot;
       const int S = (int)align_up((size_t)((P.V + CS - 1) / CS), 8);
       const size_t smem = (size_t)P.N * ((S + E - 1) / E) * sizeof(float2);
       if ((long long)P.N * S * esT > (1LL << 20) || smem > kTreeUnitSmemMax) return false;
+      if (!small && (long long)P.B * CS < sms) return false;
       if (P.B > cluster_capacity<MODE, TDT, DDT, PROBS>(dev, slot)) continue;
       cp = ClusterPlan{CS, S, 0, smem};
       return true;
@@ -257,18 +262,25 @@ bool cluster_plan(const KParams &P, int dev, ClusterPlan &cp) {
     return false;
   }
   if (MODE != MODE_CHAIN && MODE != MODE_CHAIN_GREEDY) return false;
+  // the smallest cluster whose kept slices fit, then larger ones while the
+  // slices keep at least kClusterMinSlice entries and the clusters still fit
   const int es = esT > esD ? esT : esD;
   const int keep = MODE == MODE_CHAIN ? 2 * P.gamma + 1 : P.gamma + 1;
-  for (int slot = 0; slot <= 3; ++slot) {
+  int chosen = -1;
+  ClusterPlan best{};
+  for (int slot = 0; slot < kClusterSlots; ++slot) {
     const int CS = 1 << slot;
     const int S = (int)align_up((size_t)((P.V + CS - 1) / CS), 8);
     const int rstride = (int)align_up((size_t)S * es, 16);
     if ((long long)keep * rstride > kClusterSmemMax) continue;
-    if (P.B > cluster_capacity<MODE, TDT, DDT, PROBS>(dev, slot)) return false;
-    cp = ClusterPlan{CS, S, rstride, (size_t)keep * rstride};
-    return true;
+    if (chosen >= 0 && S < kClusterMinSlice) break;
+    if (P.B > cluster_capacity<MODE, TDT, DDT, PROBS>(dev, slot)) break;
+    chosen = slot;
+    best = ClusterPlan{CS, S, rstride, (size_t)keep * rstride};
   }
-  return false;
+  if (chosen < 0) return false;
+  cp = best;
+  return true;
 }
 
 // One launch of the cluster path: B clusters of CS CTAs, a programmatic
