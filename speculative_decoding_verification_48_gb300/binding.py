@@ -374,8 +374,9 @@ def spec_tree_kv_compact(kv: torch.Tensor, base: torch.Tensor, path: torch.Tenso
 
 
 def spec_verify_wait_selftest(which: int, device=None, stream=None) -> int:
-    """Run bounded wait ``which`` (0: counter reset, 1: decision flag) on a
-    flag that nothing sets (see spec_verify_wait_selftest in spec_verify.h);
+    """Run bounded wait ``which`` (0: counter reset, 1: the decide kernel's
+    poll of tagged partials) on words that nothing sets (see
+    spec_verify_wait_selftest in spec_verify.h);
     returns the status the device reported, SV_ROW_TIMEOUT when the wait gave
     up as it should."""
     dev = torch.device(device) if device is not None else torch.device("cuda")
