@@ -856,7 +856,7 @@ __device__ void decide_draft_row(const PassParams &P, int b) {
 }
 
 template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
-__global__ void __launch_bounds__(kPassThreads, 4) sv_decide_kernel(const PassParams P) {
+__global__ void __launch_bounds__(kPassThreads, UNAL ? 3 : 4) sv_decide_kernel(const PassParams P) {
   const int b = blockIdx.x / P.H, h = blockIdx.x - b * P.H;
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     // the stats kernel has finished with its claim counters: leave them
