@@ -34,7 +34,7 @@ constexpr int kClusterMax = 8;        // largest cluster: the portable size
 constexpr int kClThreads = 512;       // chain CTAs: 16 warps, one per kept row at a time
 constexpr int kClWarps = kClThreads / 32;
 constexpr int kClParts = kClusterMax * kClWarps;  // draw parts of a cluster: at most 128
-constexpr int kClusterSmemMax = 96 * 1024;  // kept row slices per chain CTA
+constexpr int kClusterSmemMax = 128 * 1024;  // kept row slices and draw weights per chain CTA
 
 struct ClusterParams {
   const void *target;  // chain: [B, gamma+1, V]; tree: [B*N, V]
@@ -235,6 +235,8 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
   __shared__ float rowM[kMaxRows], rowZ[kMaxRows];
   __shared__ int rowI[kMaxRows];
   __shared__ float cl_w[2][kClWarps];  // this CTA's per-warp draw weights
+  __shared__ float cl_lsum[kClWarps][32];  // ... per lane (the draw's own weights)
+  __shared__ int cl_lpos[kClWarps][32];    // each lane's last element of positive weight
   __shared__ int cl_j, cl_kind;
   __shared__ int cl_x[32];  // the draft tokens, for the row's outputs
   __shared__ ResidCoef cl_rk;
@@ -412,17 +414,23 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
   const unsigned char *qrow = cl_rows + (size_t)(G1 + j) * P.rstride;
   const float Mw = kind == 1 ? rowM[g] : rk.Mp;  // the row whose probabilities weigh
   const int i0 = warp * L + lane * PER;
+  // the draw's own weights (the residual, or the bonus row) are kept in
+  // shared memory after the row slices, with each lane's sum and last
+  // positive element, so the rescan below reads them back
+  float *wbuf = reinterpret_cast<float *>(cl_rows + (size_t)(G1 + g) * P.rstride);
   float ws0 = 0.f, ws1 = 0.f;
   if (kind >= 0) {
+    int lpos = -1;
     for (int t = 0; t < PER; ++t) {
       if (i0 + t >= n) break;
-      if (kind == 0) {
-        ws0 += draw_weight<TDT, DDT, PROBS>(true, prow, qrow, i0 + t, rk, Mw);
-        ws1 += draw_weight<TDT, DDT, PROBS>(false, prow, qrow, i0 + t, rk, Mw);
-      } else {
-        ws0 += draw_weight<TDT, DDT, PROBS>(false, prow, qrow, i0 + t, rk, Mw);
-      }
+      const float w = draw_weight<TDT, DDT, PROBS>(kind == 0, prow, qrow, i0 + t, rk, Mw);
+      wbuf[i0 + t] = w;
+      ws0 += w;
+      if (w > 0.f) lpos = i0 + t;
+      if (kind == 0) ws1 += draw_weight<TDT, DDT, PROBS>(false, prow, qrow, i0 + t, rk, Mw);
     }
+    cl_lsum[warp][lane] = ws0;
+    cl_lpos[warp][lane] = lpos;
     ws0 = warp_sum(ws0);
     ws1 = warp_sum(ws1);
   }
@@ -517,14 +525,20 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
   // 7. the part's owner rescans it from shared memory and writes the row
   const ClusterDraw d = cl_draw;
   if (kind >= 0 && !d.bad && d.part / kClWarps == (int)rank && warp == d.part % kClWarps) {
-    const bool resid = kind == 0 && !d.alt;
+    // the draw's own weights were kept; p_j (a residual without mass) is
+    // weighed again
     float tsum = 0.f;
     int lastpos = -1;
-    for (int t = 0; t < PER; ++t) {
-      if (i0 + t >= n) break;
-      const float w = draw_weight<TDT, DDT, PROBS>(resid, prow, qrow, i0 + t, rk, Mw);
-      tsum += w;
-      if (w > 0.f) lastpos = i0 + t;
+    if (!d.alt) {
+      tsum = cl_lsum[warp][lane];
+      lastpos = cl_lpos[warp][lane];
+    } else {
+      for (int t = 0; t < PER; ++t) {
+        if (i0 + t >= n) break;
+        const float w = draw_weight<TDT, DDT, PROBS>(false, prow, qrow, i0 + t, rk, Mw);
+        tsum += w;
+        if (w > 0.f) lastpos = i0 + t;
+      }
     }
     float incl = tsum;
 #pragma unroll
@@ -542,7 +556,8 @@ __global__ void __launch_bounds__(kClThreads, 1) sv_cluster_chain_kernel(const C
         float acc = start;
         for (int t = 0; t < PER && kk < 0; ++t) {
           if (i0 + t >= n) break;
-          acc += draw_weight<TDT, DDT, PROBS>(resid, prow, qrow, i0 + t, rk, Mw);
+          acc += d.alt ? draw_weight<TDT, DDT, PROBS>(false, prow, qrow, i0 + t, rk, Mw)
+                       : wbuf[i0 + t];
           if (acc > d.target) kk = i0 + t;
         }
         if (kk < 0) kk = lastpos >= 0 ? lastpos : i0;

@@ -130,8 +130,10 @@ sv_status launch_pass_t(const KParams &P0, const PassLayout &L, long long total,
     (void)cudaGetLastError();
     capture = cudaStreamCaptureStatusActive;
   }
-  S.poll = capture == cudaStreamCaptureStatusNone && total >= 16LL * grid * kPassWarps &&
-           call_id < kPollCalls;
+  // Trees poll whenever the stats grid fills every SM: their few decide CTAs
+  // can then only become resident as stats CTAs leave.
+  S.poll = capture == cudaStreamCaptureStatusNone && call_id < kPollCalls &&
+           (total >= 16LL * grid * kPassWarps || (MODE == MODE_TREE && grid == cap));
   // Both kernels are programmatic dependents of the work before them: the
   // stats kernel of whatever the stream ran last (it waits on the device
   // before touching the workspace), the decide kernel of the stats kernel.
@@ -272,11 +274,14 @@ bool cluster_plan(const KParams &P, int dev, ClusterPlan &cp) {
     const int CS = 1 << slot;
     const int S = (int)align_up((size_t)((P.V + CS - 1) / CS), 8);
     const int rstride = (int)align_up((size_t)S * es, 16);
-    if ((long long)keep * rstride > kClusterSmemMax) continue;
+    // the kept slices, then (stochastic chains) the draw's weights
+    const size_t smem = (size_t)keep * rstride +
+                        (MODE == MODE_CHAIN ? align_up((size_t)S * sizeof(float), 16) : 0);
+    if (smem > (size_t)kClusterSmemMax) continue;
     if (chosen >= 0 && S < kClusterMinSlice) break;
     if (P.B > cluster_capacity<MODE, TDT, DDT, PROBS>(dev, slot)) break;
     chosen = slot;
-    best = ClusterPlan{CS, S, rstride, (size_t)keep * rstride};
+    best = ClusterPlan{CS, S, rstride, smem};
   }
   if (chosen < 0) return false;
   cp = best;

@@ -739,36 +739,88 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
   __syncthreads();
   int flags = 0;
   const Part *pb = P.part + (size_t)b * N * P.cMax;
-  if (P.cT <= 32) {
-    // Rows of at most 32 chunks: each lane holds one chunk partial of each
-    // of 8 rows, all loaded at once, so a warp's group of 8 rows costs one
-    // memory round trip.  The merge is that of warp_row_argmax: the largest
-    // value, the lowest index among chunks holding it, NaN flags the row.
-    for (int r0 = warp * 8; r0 < N; r0 += kPassWarps * 8) {
-      float2 pt[8];
+  // On polling calls the partials are merged as they arrive: every partial
+  // a lane holds must carry this call's tag (bounded; if the bound runs out
+  // anywhere in the CTA, the CTA takes the dependency wait and merges again).
+  bool polled = false;
+  if (P.poll && P.cT <= 32) {
+    bool ok = true;
+    for (int r0 = warp * 8; ok && r0 < N; r0 += kPassWarps * 8) {
+      unsigned long long w[8][2];
+      bool need[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const int r = r0 + k;
-        pt[k] = (r < N && lane < P.cT)
-                    ? part_value(pb + (size_t)r * P.cMax + lane)
-                    : make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
+        need[k] = r0 + k < N && lane < P.cT;
+        w[k][0] = w[k][1] = 0ull;
       }
+      for (int it = 0;; ++it) {
+        bool pending = false;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (need[k]) part_poll(pb + (size_t)(r0 + k) * P.cMax + lane, w[k][0], w[k][1]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          need[k] = need[k] && !part_tagged(w[k][0], w[k][1], P.part_tag);
+          pending |= need[k];
+        }
+        if (!__any_sync(0xffffffffu, pending)) break;
+        if (it >= kPollSpins) {
+          ok = false;
+          break;
+        }
+        __nanosleep(128);
+      }
+      if (!ok) break;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int r = r0 + k;  // warp-uniform
         if (r < N) {
-          if (__any_sync(0xffffffffu, isnan(pt[k].x))) flags |= SV_ROW_NONFINITE;
-          const float M = warp_max_nan(pt[k].x);
-          const int I = warp_min_int(pt[k].x == M ? __float_as_int(pt[k].y) : 0x7fffffff);
+          const float v = lane < P.cT ? __uint_as_float((unsigned)w[k][0]) : -CUDART_INF_F;
+          const int i = lane < P.cT ? (int)(unsigned)w[k][1] : 0x7fffffff;
+          if (__any_sync(0xffffffffu, isnan(v))) flags |= SV_ROW_NONFINITE;
+          const float M = warp_max_nan(v);
+          const int I = warp_min_int(v == M ? i : 0x7fffffff);
           if (lane == 0) sm.a[r] = I;
         }
       }
     }
-  } else {
-    for (int r = warp; r < N; r += kPassWarps) {
-      const float2 mi = warp_row_argmax(pb + (size_t)r * P.cMax, P.cT);
-      if (lane == 0) sm.a[r] = __float_as_int(mi.y);
-      if (isnan(mi.x)) flags |= SV_ROW_NONFINITE;
+    polled = __syncthreads_and(ok);
+    if (polled) asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    else flags = 0;
+  }
+  if (!polled) {
+    grid_dependency_wait();  // the stats kernel's partials are complete
+    if (P.cT <= 32) {
+      // Rows of at most 32 chunks: each lane holds one chunk partial of each
+      // of 8 rows, all loaded at once, so a warp's group of 8 rows costs one
+      // memory round trip.  The merge is that of warp_row_argmax: the largest
+      // value, the lowest index among chunks holding it, NaN flags the row.
+      for (int r0 = warp * 8; r0 < N; r0 += kPassWarps * 8) {
+        float2 pt[8];
+  #pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = r0 + k;
+          pt[k] = (r < N && lane < P.cT)
+                      ? part_value(pb + (size_t)r * P.cMax + lane)
+                      : make_float2(-CUDART_INF_F, __int_as_float(0x7fffffff));
+        }
+  #pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = r0 + k;  // warp-uniform
+          if (r < N) {
+            if (__any_sync(0xffffffffu, isnan(pt[k].x))) flags |= SV_ROW_NONFINITE;
+            const float M = warp_max_nan(pt[k].x);
+            const int I = warp_min_int(pt[k].x == M ? __float_as_int(pt[k].y) : 0x7fffffff);
+            if (lane == 0) sm.a[r] = I;
+          }
+        }
+      }
+    } else {
+      for (int r = warp; r < N; r += kPassWarps) {
+        const float2 mi = warp_row_argmax(pb + (size_t)r * P.cMax, P.cT);
+        if (lane == 0) sm.a[r] = __float_as_int(mi.y);
+        if (isnan(mi.x)) flags |= SV_ROW_NONFINITE;
+      }
     }
   }
   for (int n = threadIdx.x; n < N; n += kPassThreads) {
@@ -779,7 +831,9 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
     if (n == 0 ? par != -1 : (par < 0 || par >= n)) flags |= SV_ROW_BAD_TREE;
     if (n > 0 && (tok < 0 || tok >= V)) flags |= SV_ROW_BAD_TOKEN;
   }
-  if (threadIdx.x == 0 && __ldcg(P.claim_err) == __ldcg(P.epoch_cur)) flags |= SV_ROW_TIMEOUT;
+  // (a polled merge saw every partial of this call: no claim ran out)
+  if (!polled && threadIdx.x == 0 && __ldcg(P.claim_err) == __ldcg(P.epoch_cur))
+    flags |= SV_ROW_TIMEOUT;
   if (flags) atomicOr(&sm.flags, flags);
   __syncthreads();
   if (warp != 0) return;
@@ -876,8 +930,7 @@ __global__ void __launch_bounds__(kPassThreads, UNAL ? 3 : 4) sv_decide_kernel(c
   }
   if (MODE == MODE_TREE) {
     __shared__ TreeSmem sm;
-    grid_dependency_wait();  // the stats kernel's partials are complete
-    decide_tree<TDT>(P, b, sm);
+    decide_tree<TDT>(P, b, sm);  // it polls the partials or waits for the stats kernel
   } else {
     __shared__ DecideSmem sm;
     decide_chain_row<MODE, TDT, DDT, PROBS, UNAL>(P, b, h, sm);

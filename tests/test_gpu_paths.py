@@ -62,6 +62,11 @@ def test_mixed_dtypes_rows_off_grid(svp, tdt, ddt):
     TP.check_chain(svp, case)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_ragged_odd_vocabulary(svp, dtype):
+    TP.test_chain_ragged_tiles(svp, dtype, 8193)
+
+
 @pytest.mark.parametrize("gamma", [1, 31])
 def test_gamma_extremes(svp, gamma):
     TP.test_chain_gamma_extremes(svp, gamma)
