@@ -739,6 +739,14 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
   __syncthreads();
   int flags = 0;
   const Part *pb = P.part + (size_t)b * N * P.cMax;
+  // The tree arrays are inputs (the stats kernel writes neither): each
+  // thread's first node is loaded before the merge, which hides its latency.
+  const int n0 = threadIdx.x;
+  int par0 = 0, tok0 = 0;
+  if (n0 < N) {
+    par0 = __ldg(P.parent + (size_t)b * N + n0);
+    tok0 = __ldg(P.node_tokens + (size_t)b * N + n0);
+  }
   // On polling calls the partials are merged as they arrive: every partial
   // a lane holds must carry this call's tag (bounded; if the bound runs out
   // anywhere in the CTA, the CTA takes the dependency wait and merges again).
@@ -823,9 +831,9 @@ __device__ void decide_tree(const PassParams &P, int b, TreeSmem &sm) {
       }
     }
   }
-  for (int n = threadIdx.x; n < N; n += kPassThreads) {
-    const int par = __ldg(P.parent + (size_t)b * N + n);
-    const int tok = __ldg(P.node_tokens + (size_t)b * N + n);
+  for (int n = n0; n < N; n += kPassThreads) {
+    const int par = n == n0 ? par0 : __ldg(P.parent + (size_t)b * N + n);
+    const int tok = n == n0 ? tok0 : __ldg(P.node_tokens + (size_t)b * N + n);
     sm.par[n] = par;
     sm.tok[n] = tok;
     if (n == 0 ? par != -1 : (par < 0 || par >= n)) flags |= SV_ROW_BAD_TREE;

@@ -277,8 +277,10 @@ __device__ __forceinline__ void chunk_process(const ChunkRef &r, uint4 (&buf)[kC
   else chunk_reduce<DDT, UNAL>(r, buf);
 }
 
-// Dynamic work claims: kClaimStripes counters, counter s handing out the
-// chunks k = kClaimStripes * i + s in order, so all stripes advance through
+// Work claims.  Warp w of the grid takes chunk w first, without a claim;
+// the chunks after the grid's first k0 = gridDim.x * kPassWarps are claimed
+// dynamically from kClaimStripes counters, counter s handing out the chunks
+// k = k0 + kClaimStripes * i + s in order, so all stripes advance through
 // the list together (one contiguous front in memory, the list order kept)
 // while no single address takes every atomic.  A warp starts on stripe
 // (warp index mod kClaimStripes); when its stripe runs dry it reads every
@@ -286,6 +288,7 @@ __device__ __forceinline__ void chunk_process(const ChunkRef &r, uint4 (&buf)[kC
 // every stripe is exhausted.
 struct Claimer {
   int s;
+  long long k0;
 };
 
 // Flags this call (epoch E) as unfinished: its decide kernel then reports
@@ -325,7 +328,7 @@ __device__ __forceinline__ unsigned claim_issue(const PassParams &P, const Claim
 __device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, unsigned pend,
                                              unsigned long long E) {
   const int lane = lane_id();
-  long long k = (long long)__shfl_sync(0xffffffffu, pend, 0) * kClaimStripes + c.s;
+  long long k = c.k0 + (long long)__shfl_sync(0xffffffffu, pend, 0) * kClaimStripes + c.s;
   // every probe finds a stripe with chunks left or ends the loop; a claim
   // lost to a race only repeats the probe, so the bound is never reached in
   // practice — if it were, the call is flagged rather than left unfinished
@@ -336,24 +339,39 @@ __device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, un
     }
     unsigned cnt = 0xffffffffu;
     if (lane < kClaimStripes) cnt = ld_volatile_u32(P.claim + lane * kClaimStride);
-    const bool has = lane < kClaimStripes && (long long)cnt * kClaimStripes + lane < P.total;
+    const bool has = lane < kClaimStripes && c.k0 + (long long)cnt * kClaimStripes + lane < P.total;
     const unsigned m = __ballot_sync(0xffffffffu, has);
     if (!m) return -1;
     c.s = __ffs(m) - 1;
-    k = (long long)__shfl_sync(0xffffffffu, claim_issue(P, c), 0) * kClaimStripes + c.s;
+    k = c.k0 + (long long)__shfl_sync(0xffffffffu, claim_issue(P, c), 0) * kClaimStripes + c.s;
   }
   return (int)k;
 }
 
 template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
 __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassParams P) {
-  // The decide kernel may launch at once: its CTAs take the place of
-  // finished stats CTAs and wait on the device for this grid to complete.
-  grid_dependents_launch();
-  // This kernel is itself a programmatic dependent of whatever the stream
-  // ran before (typically the previous call's decide kernel): nothing of the
-  // workspace is touched before that work has completed.
+  // This kernel is a programmatic dependent of whatever the stream ran
+  // before (typically the previous call's decide kernel, or the kernel that
+  // wrote the logits): neither the inputs nor the workspace are touched
+  // before that work has completed.
   grid_dependency_wait();
+  // Only then may the decide kernel launch (its CTAs take the place of
+  // finished stats CTAs and wait on the device for this grid to complete):
+  // it reads inputs before that wait, so the work that wrote them must be
+  // complete, even where that work let its own dependents launch early.
+  grid_dependents_launch();
+  // The warp's first chunk needs no claim: its loads are in flight while
+  // the counters are checked and the first claim is made.
+  const int kw = blockIdx.x * kPassWarps + warp_id();
+  Claimer cl{kw % kClaimStripes, (long long)gridDim.x * kPassWarps};
+  uint4 b0[kChunkVecs], b1[kChunkVecs];
+  int ka = kw < P.total ? kw : -1;
+  ChunkRef ra;
+  ra.kind = CK_SKIP;
+  if (ka >= 0) {
+    ra = decode_chunk<MODE, TDT, DDT, PROBS, UNAL>(P, ka);
+    chunk_issue<TDT, DDT, UNAL>(ra, b0);
+  }
   // This call's epoch.  epoch_base is written only by this call's decide
   // kernel after this grid has completed, so every CTA reads the same value.
   const unsigned long long E = __ldcg(P.epoch_base) + 1ull;
@@ -372,13 +390,8 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
     __threadfence();
     st_release_u64(P.claim_ready, E);
   }
-  Claimer cl{(int)((blockIdx.x * kPassWarps + warp_id()) % kClaimStripes)};
   if (!stamped && !counters_reset_wait(P, E)) return;
-  uint4 b0[kChunkVecs], b1[kChunkVecs];
-  int ka = claim_resolve(P, cl, claim_issue(P, cl), E);
-  if (ka >= 0) {
-    ChunkRef ra = decode_chunk<MODE, TDT, DDT, PROBS, UNAL>(P, ka);
-    chunk_issue<TDT, DDT, UNAL>(ra, b0);
+  if (ka >= 0) {  // (a warp without a first chunk has none to claim either)
     unsigned pend = claim_issue(P, cl);  // the next claim is in flight while a chunk is reduced
     // two chunks per iteration so both buffers have static names
     while (true) {
