@@ -383,8 +383,10 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
   // Claim counters: zero and stamped valid by the previous call's decide
   // kernel, else (fresh or overwritten workspace) zeroed here by thread 0 of
   // CTA 0 while every warp waits.  The stamp is not written while this grid
-  // runs, so all warps take the same path.
-  const bool stamped = ld_acquire_u64(P.claim_stamp) == kStampValid;
+  // runs, so all warps take the same path.  A plain load suffices: the
+  // dependency wait above made the previous kernel's writes visible (an
+  // acquire would also hold this warp's claim behind its chunk loads).
+  const bool stamped = __ldcg(P.claim_stamp) == kStampValid;
   if (!stamped && blockIdx.x == 0 && threadIdx.x == 0) {
     for (int s = 0; s < kClaimStripes; ++s) P.claim[s * kClaimStride] = 0u;
     __threadfence();
