@@ -920,28 +920,28 @@ __device__ void decide_draft_row(const PassParams &P, int b) {
 template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
 __global__ void __launch_bounds__(kPassThreads, UNAL ? 3 : 4) sv_decide_kernel(const PassParams P) {
   const int b = blockIdx.x / P.H, h = blockIdx.x - b * P.H;
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    // the stats kernel has finished with its claim counters: leave them
-    // zeroed, record this call's epoch and stamp the counters valid for the
-    // next call on this workspace (which reads them after this grid ends)
-    grid_dependency_wait();
-    for (int s = 0; s < kClaimStripes; ++s) P.claim[s * kClaimStride] = 0u;
-    *P.epoch_base = __ldcg(P.epoch_cur);
-    __threadfence();
-    st_release_u64(P.claim_stamp, kStampValid);
-  }
   if (MODE == MODE_DRAFT) {
     grid_dependency_wait();  // the stats kernel's partials are complete
     const int r = blockIdx.x * kPassWarps + warp_id();  // one warp per row
     if (r < P.B) decide_draft_row<TDT>(P, r);
-    return;
-  }
-  if (MODE == MODE_TREE) {
+  } else if (MODE == MODE_TREE) {
     __shared__ TreeSmem sm;
     decide_tree<TDT>(P, b, sm);  // it polls the partials or waits for the stats kernel
   } else {
     __shared__ DecideSmem sm;
     decide_chain_row<MODE, TDT, DDT, PROBS, UNAL>(P, b, h, sm);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // After CTA 0's own row: the stats kernel has finished with its claim
+    // counters (a polling CTA 0 waits for it only here, so its row is not
+    // held up by the wait): leave them zeroed, record this call's epoch and
+    // stamp the counters valid for the next call on this workspace (which
+    // reads them after this grid ends).
+    grid_dependency_wait();
+    for (int s = 0; s < kClaimStripes; ++s) P.claim[s * kClaimStride] = 0u;
+    *P.epoch_base = __ldcg(P.epoch_cur);
+    __threadfence();
+    st_release_u64(P.claim_stamp, kStampValid);
   }
 }
 

@@ -323,29 +323,45 @@ __device__ __forceinline__ unsigned claim_issue(const PassParams &P, const Claim
   return v;
 }
 
-// The chunk of a claim made on the warp's current stripe (the one claim in
-// flight is always resolved before the warp can move to another stripe).
-__device__ __forceinline__ int claim_resolve(const PassParams &P, Claimer &c, unsigned pend,
-                                             unsigned long long E) {
+// The chunk of the claim in flight on the warp's current stripe (the one
+// claim in flight is always resolved before the warp can move to another
+// stripe), or -1 when that stripe is exhausted: lanes below kClaimStripes
+// then hold in cnt a read of every counter, issued here and first used by
+// claim_probe after the warp's current chunk, so the stripe change costs
+// the chunk no round trip.
+__device__ __forceinline__ int claim_take(const PassParams &P, const Claimer &c, unsigned pend,
+                                          unsigned &cnt) {
   const int lane = lane_id();
-  long long k = c.k0 + (long long)__shfl_sync(0xffffffffu, pend, 0) * kClaimStripes + c.s;
-  // every probe finds a stripe with chunks left or ends the loop; a claim
-  // lost to a race only repeats the probe, so the bound is never reached in
-  // practice — if it were, the call is flagged rather than left unfinished
-  for (int probe = 0; k >= P.total; ++probe) {
+  const long long k = c.k0 + (long long)__shfl_sync(0xffffffffu, pend, 0) * kClaimStripes + c.s;
+  if (k < P.total) return (int)k;
+  cnt = lane < kClaimStripes ? ld_volatile_u32(P.claim + lane * kClaimStride) : 0xffffffffu;
+  return -1;
+}
+
+// A claim on a stripe with chunks left, from the counters read by
+// claim_take (read again after a lost race); -1 once every stripe is
+// exhausted.  Every probe finds a stripe with chunks left or ends the loop;
+// a claim lost to a race only repeats the probe, so the bound is never
+// reached in practice — if it were, the call is flagged rather than left
+// unfinished.
+static __device__ __noinline__ int claim_probe(const PassParams &P, Claimer &c, unsigned cnt,
+                                               unsigned long long E) {
+  const int lane = lane_id();
+  for (int probe = 0;; ++probe) {
     if (probe == kClaimProbes) {
       claim_fail(P, E);
       return -1;
     }
-    unsigned cnt = 0xffffffffu;
-    if (lane < kClaimStripes) cnt = ld_volatile_u32(P.claim + lane * kClaimStride);
+    if (probe > 0)
+      cnt = lane < kClaimStripes ? ld_volatile_u32(P.claim + lane * kClaimStride) : 0xffffffffu;
     const bool has = lane < kClaimStripes && c.k0 + (long long)cnt * kClaimStripes + lane < P.total;
     const unsigned m = __ballot_sync(0xffffffffu, has);
     if (!m) return -1;
     c.s = __ffs(m) - 1;
-    k = c.k0 + (long long)__shfl_sync(0xffffffffu, claim_issue(P, c), 0) * kClaimStripes + c.s;
+    const long long k =
+        c.k0 + (long long)__shfl_sync(0xffffffffu, claim_issue(P, c), 0) * kClaimStripes + c.s;
+    if (k < P.total) return (int)k;
   }
-  return (int)k;
 }
 
 template <int MODE, int TDT, int DDT, bool PROBS, bool UNAL>
@@ -395,9 +411,10 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
   if (!stamped && !counters_reset_wait(P, E)) return;
   if (ka >= 0) {  // (a warp without a first chunk has none to claim either)
     unsigned pend = claim_issue(P, cl);  // the next claim is in flight while a chunk is reduced
+    unsigned cnt = 0xffffffffu;
     // two chunks per iteration so both buffers have static names
     while (true) {
-      const int kb = claim_resolve(P, cl, pend, E);
+      int kb = claim_take(P, cl, pend, cnt);
       ChunkRef rb;
       rb.kind = CK_SKIP;
       if (kb >= 0) {
@@ -406,15 +423,27 @@ __global__ void __launch_bounds__(kPassThreads, 2) sv_stats_kernel(const PassPar
         pend = claim_issue(P, cl);
       }
       chunk_process<MODE, TDT, DDT, PROBS, UNAL>(ra, b0);
-      if (kb < 0) break;
-      ka = claim_resolve(P, cl, pend, E);
+      if (kb < 0) {
+        kb = claim_probe(P, cl, cnt, E);
+        if (kb < 0) break;
+        rb = decode_chunk<MODE, TDT, DDT, PROBS, UNAL>(P, kb);
+        chunk_issue<TDT, DDT, UNAL>(rb, b1);
+        pend = claim_issue(P, cl);
+      }
+      ka = claim_take(P, cl, pend, cnt);
       if (ka >= 0) {
         ra = decode_chunk<MODE, TDT, DDT, PROBS, UNAL>(P, ka);
         chunk_issue<TDT, DDT, UNAL>(ra, b0);
         pend = claim_issue(P, cl);
       }
       chunk_process<MODE, TDT, DDT, PROBS, UNAL>(rb, b1);
-      if (ka < 0) break;
+      if (ka < 0) {
+        ka = claim_probe(P, cl, cnt, E);
+        if (ka < 0) break;
+        ra = decode_chunk<MODE, TDT, DDT, PROBS, UNAL>(P, ka);
+        chunk_issue<TDT, DDT, UNAL>(ra, b0);
+        pend = claim_issue(P, cl);
+      }
     }
   }
 }
