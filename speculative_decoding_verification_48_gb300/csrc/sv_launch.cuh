@@ -10,6 +10,7 @@
 namespace sv {
 
 constexpr int kMaxDevices = 64;
+constexpr int kTreeCarveout = 42;  // percent of the largest shared-memory carveout
 
 // Partials are polled (merged before the dependency wait) only by the first
 // kPollCalls calls of the process: their tags, below, are then all
@@ -45,18 +46,39 @@ sv_status launch_pass_t(const KParams &P0, const PassLayout &L, long long total,
   constexpr bool unaligned = UNAL;
   auto stats = sv_stats_kernel<MODE, TDT, DDT, PROBS, UNAL>;
   auto decide = sv_decide_kernel<MODE, TDT, DDT, PROBS, UNAL>;
-  static std::atomic<int> occ_cache[kMaxDevices], occd_cache[kMaxDevices];
+  static std::atomic<int> occ_cache[kMaxDevices], occd_cache[kMaxDevices], per_cache[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
   int occ = occ_cache[dev].load(std::memory_order_relaxed);
   int occd = occd_cache[dev].load(std::memory_order_relaxed);
+  int per = per_cache[dev].load(std::memory_order_relaxed);
   if (occ == 0 || occd == 0) {
+    // Tree calls keep their decide CTAs resident beside the stats kernel
+    // (below), which needs both kernels on one shared-memory carveout (an SM
+    // holding CTAs of one configuration takes no CTA of another): about
+    // 100 KB, room for two decide CTAs, leaving the L1 room for the stats
+    // kernel's loads in flight.
+    if (MODE == MODE_TREE &&
+        (cudaFuncSetAttribute(stats, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              kTreeCarveout) != cudaSuccess ||
+         cudaFuncSetAttribute(decide, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              kTreeCarveout) != cudaSuccess))
+      return SV_ERR_CUDA;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, stats, kPassThreads, 0) != cudaSuccess ||
         occ <= 0 ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occd, decide, kPassThreads, 0) !=
             cudaSuccess ||
         occd <= 0)
       return SV_ERR_CUDA;
+    // decide CTAs that fit the registers of one stats CTA (registers are
+    // allocated per warp in steps of 8 per thread)
+    cudaFuncAttributes fs, fd;
+    if (cudaFuncGetAttributes(&fs, stats) != cudaSuccess ||
+        cudaFuncGetAttributes(&fd, decide) != cudaSuccess)
+      return SV_ERR_CUDA;
+    const int regs_s = (fs.numRegs + 7) / 8 * 8, regs_d = (fd.numRegs + 7) / 8 * 8;
+    per = regs_d > 0 ? regs_s / regs_d : 0;
+    per_cache[dev].store(per, std::memory_order_relaxed);
     occ_cache[dev].store(occ, std::memory_order_relaxed);
     occd_cache[dev].store(occd, std::memory_order_relaxed);
   }
@@ -119,6 +141,19 @@ sv_status launch_pass_t(const KParams &P0, const PassLayout &L, long long total,
   const long long cap = (long long)sms * occ;
   int grid = (int)(want < cap ? want : cap);
   if (grid < 1) grid = 1;
+  // Trees whose stats grid would fill every SM leave stats slots free for
+  // their decide CTAs (one per tree; a stats slot holds the registers of
+  // `per` of them): those are then resident from the start, fetch their
+  // code during the stream and merge each tree's node rows as its partials
+  // arrive.
+  bool tree_room = false;
+  if (MODE == MODE_TREE && grid == cap && per >= 1) {
+    const long long fewer = (P0.B + per - 1) / per;
+    if (fewer * 8 <= cap) {
+      grid -= (int)fewer;
+      tree_room = true;
+    }
+  }
   // Merging as partials arrive pays off when the stats work is many times
   // what its resident warps hold: the decide CTAs then only become resident
   // in the stats kernel's tail.  On a small call they would be resident
@@ -130,10 +165,9 @@ sv_status launch_pass_t(const KParams &P0, const PassLayout &L, long long total,
     (void)cudaGetLastError();
     capture = cudaStreamCaptureStatusActive;
   }
-  // Trees poll whenever the stats grid fills every SM: their few decide CTAs
-  // can then only become resident as stats CTAs leave.
+  // Trees poll when their stats grid left room for the decide CTAs.
   S.poll = capture == cudaStreamCaptureStatusNone && call_id < kPollCalls &&
-           (total >= 16LL * grid * kPassWarps || (MODE == MODE_TREE && grid == cap));
+           (total >= 16LL * grid * kPassWarps || tree_room);
   // Both kernels are programmatic dependents of the work before them: the
   // stats kernel of whatever the stream ran last (it waits on the device
   // before touching the workspace), the decide kernel of the stats kernel.
