@@ -164,6 +164,19 @@ def test_c4_tree_f16_full(sv):
     assert ref["num_accepted"].max() >= 3
 
 
+@pytest.mark.parametrize("B,N,dtype", [(13, 96, "f16"), (5, 200, "bf16"), (1, 1024, "f16")])
+def test_trees_filling_the_grid(sv, B, N, dtype):
+    """Tree calls whose stats grid would fill every SM launch a few stats CTAs
+    fewer, so that the decide CTAs (one per tree) are resident from the start
+    and merge each tree as its partials arrive.  An odd number of trees, a
+    single tree of the largest size, and both 16-bit dtypes: bit-exact
+    against the oracle."""
+    case = W.make_tree(f"grid_trees_B{B}_N{N}", 7100 + B, B=B, N=N, V=32000, max_depth=8,
+                       dtype=dtype, p_match=0.9)
+    ref = check_tree(sv, case)
+    assert ref["num_accepted"].max() >= 1
+
+
 def test_c5_chain_probs_all_rows(sv, pool):
     """C5 in full: all 256 rows in one call (bf16 target, fp32 draft
     probabilities, forced all-accept rows drawing the bonus token)."""
