@@ -40,7 +40,9 @@
  *  - Each call enqueues its kernels as programmatic dependents
  *    (programmatic dependent launch) of the work before them in `stream`:
  *    the first kernel waits on the device for that work to complete before
- *    it touches the workspace, so stream order is kept.
+ *    it reads the inputs or touches the workspace, and only then lets the
+ *    call's second kernel start, so stream order is kept even after work
+ *    that lets its own dependents start early.
  *  - Calls may be captured into a CUDA graph.  Each replay verifies the
  *    inputs found in the captured buffers at replay time.
  *  - Row alignment is the caller's job: target row i scores draft i (the
