@@ -149,7 +149,7 @@ sv_status launch_pass_t(const KParams &P0, const PassLayout &L, long long total,
   bool tree_room = false;
   if (MODE == MODE_TREE && grid == cap && per >= 1) {
     const long long fewer = (P0.B + per - 1) / per;
-    if (fewer * 8 <= cap) {
+    if (fewer * 8 <= cap) {  // (many trees: at most an eighth of the grid is given up)
       grid -= (int)fewer;
       tree_room = true;
     }
